@@ -1,0 +1,542 @@
+#!/usr/bin/env python
+"""Benchmark of the potential-map hot path on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+  * direct map: 128x128x64 grid (1,048,576 points) at h = 0.5 A, 40,000
+    off-lattice atoms with charges in [-1, 1]  ->  pair evaluations/s;
+  * cutoff map: 200^3 grid (8,000,000 points) at h = 0.5 A, 100,000 atoms
+    uniform in [0,100)^3 A, c = 12 A, 4 A bins, 16-slot bins: on-device
+    binning then the brick map  ->  grid points/s (and useful pairs/s).
+Inputs are resident in HBM; L2 is flushed (a 256 MiB write) before every
+timed launch; each launch is timed with CUDA events on its stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own copy
+of the step (weak scaling, no collective on the data path); timings are the
+max over ranks.  ``--impl reference`` times the fp64 CPU oracle on the host
+cores instead, on bounded samples of the same direct workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "pair evals/s (direct Coulomb) and grid points/s at 12 Å cutoff, % of roofline"
+DIRECT_WL = "direct_3d"
+CUTOFF_WL = "cutoff_uniform"
+CAPACITY = 16
+FLUSH_BYTES = 256 << 20
+
+
+def env_rank():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def config_dict(wd, wc):
+    return {
+        "workload": f"direct {wd.shape[0]}x{wd.shape[1]}x{wd.shape[2]} grid, {wd.n_atoms} atoms, h={wd.h} A; "
+        f"cutoff {wc.shape[0]}x{wc.shape[1]}x{wc.shape[2]} grid, {wc.n_atoms} atoms, c={wc.cutoff} A, "
+        f"{wc.bin_size} A bins",
+        "direct": {"grid": list(wd.shape), "atoms": wd.n_atoms, "h": wd.h, "pairs": wd.n_pairs,
+                   "description": wd.description},
+        "cutoff": {"grid": list(wc.shape), "atoms": wc.n_atoms, "h": wc.h, "cutoff": wc.cutoff,
+                   "bin_size": wc.bin_size, "capacity": CAPACITY, "brick": [8, 8, 8],
+                   "description": wc.description},
+        "l2": "flushed before every timed launch (256 MiB write)",
+        "parallelism": "one independent copy per rank (weak scaling)",
+    }
+
+
+# ---------------------------------------------------------------------------
+# multi-rank helpers (also exercised by tests/test_bench_ranks.py with gloo)
+
+def max_over_ranks(values, device=None):
+    """Elementwise max of a list of floats over all ranks (identity at world size 1)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_id}", "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", f"-lms={period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        self.t_begin = None
+        self.t_end = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_begin(self):
+        self.t_begin = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if self.t_begin is not None and not (self.t_begin <= ts <= (self.t_end or ts)):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(CLOCK_FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "power_w_max": max(power) if power else None,
+            "reasons": sorted(reasons),
+            "samples": len(sm),
+        }
+
+
+def gpu_id_for(torch, device) -> str:
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        if uuid:
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[device.index]
+    return str(device.index)
+
+
+# ---------------------------------------------------------------------------
+# CPU baselines (the fp64 oracle, as it stands)
+
+def oracle_direct_rate(wd, target_s: float, threads: int, seed: int = 99):
+    """Times the oracle's direct sum on a sample of grid points sized for
+    about target_s seconds; returns (pairs/s, n_points, seconds)."""
+    import oracle
+    import workloads
+
+    n_pts = 64
+    while True:
+        pts = workloads.sample_points(wd.shape, n_pts, seed=seed)
+        t0 = time.perf_counter()
+        oracle.direct(wd.atoms, wd.shape, wd.origin, wd.h, points=pts, threads=threads, with_bound=False)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * target_s or n_pts >= wd.n_points:
+            return n_pts * wd.n_atoms / dt, n_pts, dt
+        n_pts = min(wd.n_points, int(n_pts * max(2.0, min(16.0, target_s / max(dt, 1e-3)))))
+
+
+def oracle_cutoff_rate(wc, target_s: float, threads: int, seed: int = 98):
+    import oracle
+    import workloads
+
+    n_pts = 64
+    while True:
+        pts = workloads.sample_points(wc.shape, n_pts, seed=seed)
+        t0 = time.perf_counter()
+        oracle.cutoff_binned(wc.atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, points=pts,
+                             threads=threads, with_bound=False)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * target_s or n_pts >= wc.n_points:
+            return n_pts / dt, n_pts, dt
+        n_pts = min(wc.n_points, int(n_pts * max(2.0, min(16.0, target_s / max(dt, 1e-3)))))
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+
+def run_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return 0
+    import oracle  # noqa: F401  (built on first use)
+    import workloads
+
+    wd = workloads.make(DIRECT_WL)
+    wc = workloads.make(CUTOFF_WL)
+    threads = host_threads()
+    # size one step for about 1.5 s so that warm-up + steps end within minutes
+    _, n_pts, _ = oracle_direct_rate(wd, 1.5, threads)
+    pts = workloads.sample_points(wd.shape, n_pts, seed=99)
+    import oracle as orc
+
+    times = []
+    for step in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        orc.direct(wd.atoms, wd.shape, wd.origin, wd.h, points=pts, threads=threads, with_bound=False)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+    t = sum(times)
+    value = n_pts * wd.n_atoms * len(times) / t
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "pair evals/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * t / len(times),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": config_dict(wd, wc),
+        "cpu_baseline": {"value": value, "unit": "pair evals/s", "cores": threads, "kind": "oracle",
+                         "sample": f"direct sum at {n_pts} seeded grid points of the {wd.shape} grid x "
+                                   f"{wd.n_atoms} atoms per step"},
+        "e2e": {"value": value, "unit": "pair evals/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+def traffic_from_profile(kernel: str, source: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    kernel's source is unchanged since it was captured (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+        with open(os.path.join(ROOT, source), "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()
+    except (OSError, ValueError, AttributeError):
+        return None
+    if not rec or rec.get("source_sha1") != sha:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = env_rank()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device (use --impl reference for the CPU oracle)")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist.init_process_group("nccl", rank=rank, world_size=world, device_id=device)
+
+    import direct_coulomb_summation_gb300 as cp
+    import workloads
+
+    lib = cp.library()
+    props = torch.cuda.get_device_properties(device)
+    n_sm = props.multi_processor_count
+
+    wd = workloads.make(DIRECT_WL)
+    wc = workloads.make(CUTOFF_WL)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    ad = torch.from_numpy(wd.atoms).to(device)
+    Vd = torch.empty((wd.shape[2], wd.shape[1], wd.shape[0]), dtype=torch.float32, device=device)
+    ac = torch.from_numpy(wc.atoms).to(device)
+    Vc = torch.empty((wc.shape[2], wc.shape[1], wc.shape[0]), dtype=torch.float32, device=device)
+    ws_bytes = cp.cutoff_workspace_bytes(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    gd = cp._grid(wd.shape, wd.origin, wd.h)
+    gc = cp._grid(wc.shape, wc.origin, wc.h)
+    cut = [float(np.float32(wc.cutoff)), float(np.float32(wc.bin_size)), CAPACITY]
+
+    def call(rc, where):
+        if rc != 0:
+            raise cp.CpError(rc, where)
+
+    def run_direct():
+        call(lib.cp_direct(ad.data_ptr(), wd.n_atoms, *gd, Vd.data_ptr(), sh), "cp_direct")
+
+    def run_bin():
+        call(lib.cp_bin_atoms(ac.data_ptr(), wc.n_atoms, *gc, *cut, ws.data_ptr(), ws_bytes, sh), "cp_bin_atoms")
+
+    def run_map():
+        call(lib.cp_cutoff_map(ac.data_ptr(), wc.n_atoms, *gc, *cut, ws.data_ptr(), ws_bytes, Vc.data_ptr(), sh),
+             "cp_cutoff_map")
+
+    # roofline denominators: per-SM pipe rates measured on this GPU
+    r_mufu, _ = cp.probe_pipe_rate("mufu_rsqrt", 32, 4096)
+    r_ffma, _ = cp.probe_pipe_rate("ffma", 32, 4096)
+    # cutoff work accounting (not timed)
+    counts = cp.cutoff_pair_counts(ac, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY, workspace=ws)
+
+    sampler = ClockSampler(gpu_id_for(torch, device))
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        run_direct()
+        flush.fill_(2)
+        run_bin()
+        run_map()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    launches0 = lib.cp_launch_count()
+    barrier(device)
+    torch.cuda.synchronize()
+    sampler.mark_begin()
+    t_wall0 = time.perf_counter()
+    for k in range(args.steps):
+        e = ev[k]
+        flush.fill_(k & 0x7F)
+        e[0].record(stream)
+        run_direct()
+        e[1].record(stream)
+        flush.fill_((k + 64) & 0x7F)
+        e[2].record(stream)
+        run_bin()
+        e[3].record(stream)
+        run_map()
+        e[4].record(stream)
+    torch.cuda.synchronize()
+    barrier(device)
+    t_wall = time.perf_counter() - t_wall0
+    sampler.mark_end()
+    launches = lib.cp_launch_count() - launches0
+    clocks = sampler.stop()
+    status = cp.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} after the timed steps")
+
+    t_direct = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    t_bin = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+    t_map = sum(e[3].elapsed_time(e[4]) for e in ev) / 1e3
+    t_direct, t_bin, t_map, t_wall = max_over_ranks([t_direct, t_bin, t_map, t_wall], device)
+    K = args.steps
+    direct_pairs = float(wd.n_pairs) * world * K
+    direct_rate = direct_pairs / t_direct
+    t_cut = t_bin + t_map
+    points_rate = float(wc.n_points) * world * K / t_cut
+
+    # rooflines -------------------------------------------------------------
+    f_mhz = clocks.get("sm_mhz") or 2070.0
+    clock_basis = "median SM clock sampled during the timed steps" if clocks.get("sm_mhz") else "max SM clock"
+    # direct: every pair needs one MUFU rsqrt and at least two FP32 FMAs
+    per_sm_direct = min(r_mufu, r_ffma / 2.0)
+    peak_direct = per_sm_direct * n_sm * f_mhz * 1e6 * world
+    achieved_direct = direct_rate
+    # cutoff: a useful pair needs one MUFU rsqrt and about 8 issue slots
+    # (dx, r^2, compare, two polynomial FMAs, subtract, accumulate + MUFU issue)
+    per_sm_useful = min(r_mufu, 128.0 / 8.0, r_ffma / 7.0)
+    useful_rate = counts["useful"] * world * K / t_map
+    peak_useful = per_sm_useful * n_sm * f_mhz * 1e6 * world
+    # binning: HBM bytes it must move at least (atoms in, bin-sorted atoms and
+    # indices out, counts and starts, fixed-capacity slots out)
+    L = cp.cutoff_layout(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY)
+    bin_bytes = 16 * wc.n_atoms * 2 + 4 * wc.n_atoms + 8 * int(L.nbins) + 16 * CAPACITY * int(L.nbins)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    hbm_basis = "of measured" if "hbm_gbs" in peaks else "of fallback"
+
+    # end to end through the public API with host buffers ---------------------
+    host_atoms_d = torch.from_numpy(wd.atoms).pin_memory()
+    host_out_d = torch.empty(Vd.shape, dtype=torch.float32, pin_memory=True)
+    host_atoms_c = torch.from_numpy(wc.atoms).pin_memory()
+    host_out_c = torch.empty(Vc.shape, dtype=torch.float32, pin_memory=True)
+    n_e2e = max(3, min(K, 10))
+    cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
+    t_e2e_d = (time.perf_counter() - t0) / n_e2e
+    cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY, workspace=ws, out=Vc,
+              host_out=host_out_c)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY, workspace=ws, out=Vc,
+                  host_out=host_out_c)
+    t_e2e_c = (time.perf_counter() - t0) / n_e2e
+    t_e2e_d, t_e2e_c = max_over_ranks([t_e2e_d, t_e2e_c], device)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    # CPU baseline: the oracle on this host's cores, bounded samples
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        threads = host_threads()
+        rate, n_pts, dt = oracle_direct_rate(wd, args.cpu_seconds, threads)
+        crate, c_pts, cdt = oracle_cutoff_rate(wc, args.cpu_seconds / 2, threads)
+        cpu = {"value": rate, "unit": "pair evals/s", "cores": threads, "kind": "oracle",
+               "sample": f"fp64 direct sum at {n_pts} seeded grid points of the {tuple(wd.shape)} grid x "
+                         f"{wd.n_atoms} atoms ({dt:.1f} s)",
+               "cutoff": {"value": crate, "unit": "grid points/s",
+                          "sample": f"fp64 binned cutoff sum at {c_pts} seeded points ({cdt:.1f} s)"}}
+
+    traffic = traffic_from_profile("direct_kernel", "direct_coulomb_summation_gb300/csrc/cp_direct.cu")
+    line = {
+        "metric": METRIC,
+        "value": direct_rate,
+        "unit": "pair evals/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * (t_direct + t_cut) / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": config_dict(wd, wc),
+        "roofline": {
+            "bound": "alu",
+            "kernel": "direct_kernel (cp_direct)",
+            "achieved": achieved_direct,
+            "peak": peak_direct,
+            "unit": "pair evals/s",
+            "frac": achieved_direct / peak_direct,
+            "traffic": traffic,
+            "peak_basis": f"{n_sm} SMs x {per_sm_direct:.2f} pairs/clk/SM (measured MUFU rsqrt "
+                          f"{r_mufu:.2f}/clk/SM, FFMA {r_ffma:.1f}/clk/SM) x {f_mhz:.0f} MHz ({clock_basis})",
+        },
+        "direct": {
+            "pair_evals_per_s": direct_rate,
+            "grid_points_per_s": float(wd.n_points) * world * K / t_direct,
+            "ms": 1e3 * t_direct / K,
+        },
+        "cutoff": {
+            "grid_points_per_s": points_rate,
+            "useful_pairs_per_s": counts["useful"] * world * K / t_cut,
+            "evaluated_pairs_per_s": counts["evaluated"] * world * K / t_cut,
+            "examined_pairs_per_s": counts["examined"] * world * K / t_cut,
+            "pairs_per_step": counts,
+            "ms": 1e3 * t_cut / K,
+            "ms_binning": 1e3 * t_bin / K,
+            "ms_map": 1e3 * t_map / K,
+            "roofline_map": {
+                "bound": "alu", "kernel": "cutoff_brick_kernel (cp_cutoff_map)",
+                "achieved": useful_rate, "peak": peak_useful, "unit": "useful pair evals/s",
+                "frac": useful_rate / peak_useful,
+                "time_vs_useful_pair_roofline": peak_useful / useful_rate,
+                "peak_basis": f"{n_sm} SMs x {per_sm_useful:.2f} useful pairs/clk/SM x {f_mhz:.0f} MHz",
+            },
+            "roofline_binning": {
+                "bound": "hbm", "achieved": bin_bytes * world * K / t_bin / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                "frac": bin_bytes * world * K / t_bin / 1e9 / hbm_peak, "traffic": None,
+                "algorithmic_bytes": bin_bytes, "peak_basis": f"hbm_gbs {hbm_basis}",
+            },
+        },
+        "cpu_baseline": cpu,
+        "e2e": {
+            "value": float(wd.n_pairs) * world / t_e2e_d,
+            "unit": "pair evals/s",
+            "h2d_bytes_per_step": int(wd.atoms.nbytes),
+            "d2h_bytes_per_step": int(Vd.numel() * 4),
+            "cutoff_grid_points_per_s": float(wc.n_points) * world / t_e2e_c,
+            "cutoff_h2d_bytes": int(wc.atoms.nbytes),
+            "cutoff_d2h_bytes": int(Vc.numel() * 4),
+            "how": "public Python API with pinned host atoms in, host V out; wall clock per call incl. copies",
+        },
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "wall_ms_per_step": 1e3 * t_wall / K,
+        "device": props.name,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

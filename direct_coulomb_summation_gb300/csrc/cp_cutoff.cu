@@ -1,0 +1,655 @@
+// cp_cutoff.cu -- cutoff summation of the switched term on sm_103a.
+//
+// Binning (Input Binning lecture, slides "Pseudo Code of an Implementation"
+// (28), "Coalesced Global Memory Access to Atom Data" (33), "Handling
+// Overfull Bins" (34); PMPP ch.18 notes section 18.5 BinTable) runs on the
+// GPU as a counting sort:
+//   clear -> count (atomic per-bin counters, each atom keeps its arrival
+//   rank) -> exclusive scan (per-block scans + one scan of block sums) ->
+//   scatter (input index to bin-sorted position) -> per-bin sort by input
+//   index (one warp per bin, rank by comparison) and pack: the first K atoms
+//   of each bin into its fixed-capacity slots, every atom into the
+//   bin-sorted (CSR) array.  Results are deterministic: within a bin the
+//   order is ascending input index whatever order the atomics ran in.
+//
+// The map (slides "Details on Small Bin Design" (30), "Tiling Atom Data"
+// (32), "GPU Thread Coarsening" (36), "GPU Thread Inner Loop" (37)): one CTA
+// per 8x8x8-point brick.  A producer warp walks the brick's neighbourhood
+// offset list (x-runs of bins, passed as a kernel parameter) and streams
+// each run's fixed-capacity slots -- then the overflow atoms of overfull
+// bins from the CSR array -- into a ring of shared-memory stages with 1-D
+// TMA bulk copies.  Four consumer warps own 4x4x... points: warp w covers an
+// 8x4x4 sub-box of the brick and each lane 4 consecutive x points.  For 32
+// slots at a time a warp tests every atom against its sub-box (distance to
+// the box < c) and keeps a ballot mask; only atoms that can reach one of
+// its points go through the pair loop, where the switched term
+// q * (rsqrt(r^2) - (GC0 + r^2 (GC1 + r^2 GC2))) is added for r^2 < c^2.
+// Pads (unused slots) sit at 1e18 A and never pass the sub-box test, which
+// replaces the lecture's stop-at-the-first-empty-slot rule.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstring>
+
+#include "cp_device.cuh"
+#include "cp_internal.h"
+
+namespace cpmap {
+
+// ---------------------------------------------------------------------------
+// binning kernels
+
+struct BinParams {
+    const float4 *atoms;
+    int n;
+    int nb[3];
+    float bo[3];
+    float b;
+    int nbins;
+    int K;
+    int *count;
+    int *start;
+    int *csr_index;
+    float4 *csr_atoms;
+    float4 *padded;
+    int *stats;  // [0] binned, [1] dropped, [2] overflow atoms, [3] max bin count
+    int2 *bin_rank;
+    int *block_sums;
+    int *block_prefix;
+};
+
+// fp32 bin coordinate: floor(float(float(a - bo) / b)), -1 outside [0, nb)
+// (NaN fails both comparisons).
+__device__ __forceinline__ int bin_axis(float a, float bo, float b, int nb) {
+    const float t = __fsub_rn(a, bo);
+    const float u = __fdiv_rn(t, b);
+    const float f = floorf(u);
+    return (f >= 0.0f && f < (float)nb) ? (int)f : -1;
+}
+
+__global__ void bin_clear_kernel(const __grid_constant__ BinParams p) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.nbins; i += stride) p.count[i] = 0;
+    if (blockIdx.x == 0 && threadIdx.x < 8) p.stats[threadIdx.x] = 0;
+}
+
+__global__ void bin_count_kernel(const __grid_constant__ BinParams p) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.n) return;
+    const float4 a = p.atoms[i];
+    const int ux = bin_axis(a.x, p.bo[0], p.b, p.nb[0]);
+    const int uy = bin_axis(a.y, p.bo[1], p.b, p.nb[1]);
+    const int uz = bin_axis(a.z, p.bo[2], p.b, p.nb[2]);
+    int bin = -1, rank = 0;
+    if (ux >= 0 && uy >= 0 && uz >= 0) {
+        bin = (uz * p.nb[1] + uy) * p.nb[0] + ux;
+        rank = atomicAdd(&p.count[bin], 1);
+    } else {
+        atomicAdd(&p.stats[1], 1);
+    }
+    p.bin_rank[i] = make_int2(bin, rank);
+}
+
+// Exclusive scan of count within blocks of kScanBlock bins (256 threads x 8);
+// local results go to start[], block totals to block_sums[].
+__global__ void __launch_bounds__(256) bin_scan_local_kernel(const __grid_constant__ BinParams p) {
+    __shared__ int warp_tot[8];
+    const int base = blockIdx.x * kScanBlock + threadIdx.x * 8;
+    int v[8];
+    int sum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        v[k] = (base + k < p.nbins) ? p.count[base + k] : 0;
+        sum += v[k];
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int warp_off = 0, block_tot = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        warp_off += (w < warp) ? warp_tot[w] : 0;
+        block_tot += warp_tot[w];
+    }
+    int run = warp_off + incl - sum;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (base + k < p.nbins) p.start[base + k] = run;
+        run += v[k];
+    }
+    if (threadIdx.x == 0) p.block_sums[blockIdx.x] = block_tot;
+}
+
+// One CTA: exclusive scan of the block totals; also start[nbins] and the
+// binned-atom count.
+__global__ void __launch_bounds__(1024) bin_scan_blocks_kernel(const __grid_constant__ BinParams p, int nblk) {
+    __shared__ int warp_tot[32];
+    const int base = threadIdx.x * 8;
+    int v[8];
+    int sum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        v[k] = (base + k < nblk) ? p.block_sums[base + k] : 0;
+        sum += v[k];
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int warp_off = 0, total = 0;
+    for (int w = 0; w < 32; ++w) {
+        warp_off += (w < warp) ? warp_tot[w] : 0;
+        total += warp_tot[w];
+    }
+    int run = warp_off + incl - sum;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (base + k < nblk) p.block_prefix[base + k] = run;
+        run += v[k];
+    }
+    if (threadIdx.x == 0) {
+        p.start[p.nbins] = total;
+        p.stats[0] = total;
+    }
+}
+
+__global__ void bin_scatter_kernel(const __grid_constant__ BinParams p) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.n) return;
+    const int2 br = p.bin_rank[i];
+    if (br.x < 0) return;
+    const int pos = p.start[br.x] + p.block_prefix[br.x / kScanBlock] + br.y;
+    p.csr_index[pos] = i;
+}
+
+// One warp per bin: rank the bin's input indices by comparison, write the
+// bin-sorted atoms and indices and the fixed-capacity slots (pads after the
+// last atom), and the final start[] entry.  8 bins per 256-thread block.
+__global__ void __launch_bounds__(256) bin_sort_pack_kernel(const __grid_constant__ BinParams p) {
+    __shared__ int blk_overflow, blk_max;
+    if (threadIdx.x == 0) {
+        blk_overflow = 0;
+        blk_max = 0;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int bin = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (bin < p.nbins) {
+        const int n = p.count[bin];
+        const int s = p.start[bin] + p.block_prefix[bin / kScanBlock];
+        int *tmp = reinterpret_cast<int *>(p.bin_rank);  // free after the scatter
+        for (int c0 = 0; c0 < n; c0 += 32) {
+            const int e = (c0 + lane < n) ? p.csr_index[s + c0 + lane] : INT_MAX;
+            int rank = 0;
+            for (int c1 = 0; c1 < n; c1 += 32) {
+                const int f = (c1 + lane < n) ? p.csr_index[s + c1 + lane] : INT_MAX;
+                const int m = min(32, n - c1);
+                for (int k = 0; k < m; ++k) rank += (__shfl_sync(0xffffffffu, f, k) < e) ? 1 : 0;
+            }
+            if (c0 + lane < n) {
+                const float4 a = p.atoms[e];
+                tmp[s + rank] = e;
+                p.csr_atoms[s + rank] = a;
+                if (rank < p.K) p.padded[(long long)bin * p.K + rank] = a;
+            }
+        }
+        __syncwarp();
+        for (int k = lane; k < n; k += 32) p.csr_index[s + k] = tmp[s + k];
+        for (int k = n + lane; k < p.K; k += 32)
+            p.padded[(long long)bin * p.K + k] = make_float4(kPadCoord, kPadCoord, kPadCoord, 0.0f);
+        __syncwarp();
+        if (lane == 0) {
+            p.start[bin] = s;
+            if (n > p.K) atomicAdd(&blk_overflow, n - p.K);
+            atomicMax(&blk_max, n);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (blk_overflow) atomicAdd(&p.stats[2], blk_overflow);
+        atomicMax(&p.stats[3], blk_max);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// brick kernel
+
+constexpr int kBrickConsumerWarps = 4;
+constexpr int kBrickThreads = 32 * (kBrickConsumerWarps + 1);  // + 1 producer warp
+constexpr int kBrickStages = 8;
+
+struct BrickParams {
+    int nx, ny, nz;
+    float ox, oy, oz, h;
+    float c2, cull2, gc0, gc1, gc2;
+    int nb[3];
+    int m;
+    double h64, b64;
+    int nbr[3];  // bricks per axis
+    const float4 *padded;
+    const int *count;
+    const int *start;
+    const float4 *csr_atoms;
+    float *V;
+    unsigned int *status;
+    unsigned long long *counts;  // pair-counting variant only: [3] see cp_cutoff_pair_counts
+    int n_runs;
+    int runs[kMaxRuns];  // packed int8 (dy, dz, dx_lo, dx_hi)
+};
+
+__device__ __forceinline__ int brick_home_dev(int brick, int m, double h, double b) {
+    const double t = __dmul_rn(8.0 * (double)brick, h);
+    return m + (int)floor(__ddiv_rn(t, b));
+}
+
+template <int K, bool VEC, bool COUNT>
+__global__ void __launch_bounds__(kBrickThreads) cutoff_brick_kernel(const __grid_constant__ BrickParams p) {
+    constexpr int kStageSlots = kRunMaxBins * K;
+    __shared__ __align__(128) float4 ring[kBrickStages][kStageSlots];
+    __shared__ uint64_t full[kBrickStages], empty[kBrickStages];
+    __shared__ volatile int stage_n[kBrickStages];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int brick = blockIdx.x;
+    const int bx = brick % p.nbr[0];
+    const int by = (brick / p.nbr[0]) % p.nbr[1];
+    const int bz = brick / (p.nbr[0] * p.nbr[1]);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBrickStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kBrickConsumerWarps);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (warp == kBrickConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        const int hx = brick_home_dev(bx, p.m, p.h64, p.b64);
+        const int hy = brick_home_dev(by, p.m, p.h64, p.b64);
+        const int hz = brick_home_dev(bz, p.m, p.h64, p.b64);
+        int seq = 0;
+        bool ok = true;
+        // lane 0 only: next stage, after its previous contents are consumed
+        auto acquire_stage = [&]() -> int {
+            const int s = seq % kBrickStages;
+            const int use = seq / kBrickStages;
+            if (use > 0 && ok) ok = mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), p.status);
+            return s;
+        };
+        auto emit = [&](const float4 *src, int nslots) {
+            const int s = acquire_stage();
+            if (ok) {
+                stage_n[s] = nslots;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)nslots * 16u);
+                bulk_g2s(&ring[s][0], src, (uint32_t)nslots * 16u, &full[s]);
+            }
+            ++seq;
+        };
+        for (int pass = 0; pass < 2; ++pass) {
+            for (int r = 0; r < p.n_runs && ok; ++r) {
+                const int code = p.runs[r];
+                const int dy = (int)(signed char)(code & 0xff);
+                const int dz = (int)(signed char)((code >> 8) & 0xff);
+                const int dxl = (int)(signed char)((code >> 16) & 0xff);
+                const int dxh = (int)(signed char)((code >> 24) & 0xff);
+                const int uy = hy + dy, uz = hz + dz;
+                if (uy < 0 || uy >= p.nb[1] || uz < 0 || uz >= p.nb[2]) continue;
+                const int xlo = max(hx + dxl, 0), xhi = min(hx + dxh, p.nb[0] - 1);
+                if (xlo > xhi) continue;
+                const int first = (uz * p.nb[1] + uy) * p.nb[0] + xlo;
+                const int nbin = xhi - xlo + 1;
+                const int cnt = lane < nbin ? p.count[first + lane] : 0;
+                if (pass == 0) {
+                    const unsigned nz = __ballot_sync(0xffffffffu, cnt > 0);
+                    if (nz != 0u) {
+                        const int l0 = __ffs(nz) - 1, l1 = 31 - __clz(nz);
+                        if (lane == 0) emit(p.padded + (long long)(first + l0) * K, (l1 - l0 + 1) * K);
+                    }
+                } else {
+                    const int st = lane < nbin ? p.start[first + lane] : 0;
+                    unsigned ov = __ballot_sync(0xffffffffu, cnt > K);
+                    while (ov != 0u) {
+                        const int j = __ffs(ov) - 1;
+                        ov &= ov - 1u;
+                        const int cj = __shfl_sync(0xffffffffu, cnt, j);
+                        const int sj = __shfl_sync(0xffffffffu, st, j);
+                        if (lane == 0) {
+                            for (int off = K; off < cj && ok; off += kStageSlots)
+                                emit(p.csr_atoms + sj + off, min(kStageSlots, cj - off));
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                seq = __shfl_sync(0xffffffffu, seq, 0);
+            }
+        }
+        if (lane == 0) {  // end of stream
+            const int s = acquire_stage();
+            stage_n[s] = -1;
+            mbar_arrive(&full[s]);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // this lane's points: x = 8bx + xq .. +3, y = 8by + yy, z = 8bz + zz
+    const int xq = (lane & 1) * 4;
+    const int yy = (warp & 1) * 4 + ((lane >> 1) & 3);
+    const int zz = (warp >> 1) * 4 + (lane >> 3);
+    const int i0 = kBrick * bx + xq, j = kBrick * by + yy, k = kBrick * bz + zz;
+    float x[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) x[c] = fmaf((float)(i0 + c), p.h, p.ox);
+    const float y = fmaf((float)j, p.h, p.oy);
+    const float z = fmaf((float)k, p.h, p.oz);
+    // the warp's sub-box (8 x 4 x 4 points), from the same coordinate formula
+    const float lox = fmaf((float)(kBrick * bx), p.h, p.ox), hix = fmaf((float)(kBrick * bx + 7), p.h, p.ox);
+    const int jb = kBrick * by + (warp & 1) * 4, kb = kBrick * bz + (warp >> 1) * 4;
+    const float loy = fmaf((float)jb, p.h, p.oy), hiy = fmaf((float)(jb + 3), p.h, p.oy);
+    const float loz = fmaf((float)kb, p.h, p.oz), hiz = fmaf((float)(kb + 3), p.h, p.oz);
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    unsigned long long n_real = 0, n_near = 0, n_useful = 0;  // COUNT only
+    for (int seq = 0;; ++seq) {
+        const int s = seq % kBrickStages;
+        if (!mbar_wait(&full[s], (uint32_t)((seq / kBrickStages) & 1), p.status)) break;
+        const int n = stage_n[s];
+        if (n < 0) break;
+        const float4 *slots = &ring[s][0];
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int base = 0; base < n; base += 32) {
+            bool near = false;
+            if (base + lane < n) {
+                const float4 a = slots[base + lane];
+                const float ex = fmaxf(fmaxf(lox - a.x, a.x - hix), 0.0f);
+                const float ey = fmaxf(fmaxf(loy - a.y, a.y - hiy), 0.0f);
+                const float ez = fmaxf(fmaxf(loz - a.z, a.z - hiz), 0.0f);
+                near = fmaf(ex, ex, fmaf(ey, ey, ez * ez)) < p.cull2;
+                if (COUNT && a.x < 1.0e17f) ++n_real;
+            }
+            unsigned mask = __ballot_sync(0xffffffffu, near);
+            if (COUNT && lane == 0) n_near += __popc(mask);
+            while (mask != 0u) {
+                const int t = __ffs(mask) - 1;
+                mask &= mask - 1u;
+                const float4 a = slots[base + t];  // broadcast
+                const float dy = y - a.y, dz = z - a.z;
+                const float dyz2 = fmaf(dy, dy, dz * dz);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float dx = x[c] - a.x;
+                    const float r2 = fmaf(dx, dx, dyz2);
+                    const float g = fmaf(fmaf(r2, p.gc2, p.gc1), r2, p.gc0);
+                    const float e = sfu_rsqrt(r2) - g;
+                    if (r2 < p.c2) part[c] = fmaf(a.w, e, part[c]);
+                    if (COUNT && r2 < p.c2 && i0 + c < p.nx && j < p.ny && k < p.nz) ++n_useful;
+                }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c] += part[c];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    if (COUNT) {
+        // per warp: real atoms seen and atoms past the sub-box test, each
+        // examined against the warp's 128 points; useful = pairs with r < c
+        // at stored points
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            n_real += __shfl_down_sync(0xffffffffu, n_real, o);
+            n_useful += __shfl_down_sync(0xffffffffu, n_useful, o);
+        }
+        if (lane == 0) {
+            atomicAdd(&p.counts[0], n_useful);
+            atomicAdd(&p.counts[1], n_near * 128ull);
+            atomicAdd(&p.counts[2], n_real * 128ull);
+        }
+        return;
+    }
+    if (j < p.ny && k < p.nz) {
+        float *row = p.V + ((long long)k * p.ny + j) * p.nx;
+        if (VEC) {
+            if (i0 < p.nx) *reinterpret_cast<float4 *>(row + i0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (i0 + c < p.nx) row[i0 + c] = acc[c];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+namespace {
+
+struct Prepared {
+    Grid g;
+    BinGeom bg;
+    cp_cutoff_layout L;
+    BinParams bp;
+};
+
+int prepare(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff,
+            float bin_size, int capacity, void *workspace, size_t workspace_bytes, Prepared *out) {
+    int rc = check_grid(nx, ny, nz, origin, h, &out->g);
+    if (rc) return rc;
+    if (n_atoms < 0 || (n_atoms > 0 && !atoms) || !workspace) return CP_ERR_INVALID_ARGUMENT;
+    rc = check_cutoff_args(out->g, cutoff, bin_size, capacity);
+    if (rc) return rc;
+    if (n_atoms > 0 && !aligned(atoms, 16)) return CP_ERR_MISALIGNED;
+    if (!aligned(workspace, 256)) return CP_ERR_MISALIGNED;
+    rc = make_bin_geometry(out->g, cutoff, bin_size, &out->bg);
+    if (rc) return rc;
+    rc = make_layout(n_atoms, out->bg, capacity, &out->L);
+    if (rc) return rc;
+    if (workspace_bytes < out->L.total_bytes) return CP_ERR_WORKSPACE_TOO_SMALL;
+    if ((long long)out->bg.nbins * capacity > INT_MAX) return CP_ERR_TOO_LARGE;
+    char *ws = static_cast<char *>(workspace);
+    BinParams &b = out->bp;
+    b.atoms = reinterpret_cast<const float4 *>(atoms);
+    b.n = n_atoms;
+    for (int d = 0; d < 3; ++d) {
+        b.nb[d] = out->bg.nb[d];
+        b.bo[d] = out->bg.bo[d];
+    }
+    b.b = bin_size;
+    b.nbins = (int)out->bg.nbins;
+    b.K = capacity;
+    b.count = reinterpret_cast<int *>(ws + out->L.off_count);
+    b.start = reinterpret_cast<int *>(ws + out->L.off_start);
+    b.csr_index = reinterpret_cast<int *>(ws + out->L.off_csr_index);
+    b.csr_atoms = reinterpret_cast<float4 *>(ws + out->L.off_csr_atoms);
+    b.padded = reinterpret_cast<float4 *>(ws + out->L.off_padded);
+    b.stats = reinterpret_cast<int *>(ws + out->L.off_stats);
+    const size_t n = (size_t)n_atoms;
+    const size_t nblk = ((size_t)out->bg.nbins + kScanBlock - 1) / kScanBlock;
+    size_t off = out->L.off_scratch;
+    b.bin_rank = reinterpret_cast<int2 *>(ws + off);
+    off += (8 * n + 255) & ~(size_t)255;
+    b.block_sums = reinterpret_cast<int *>(ws + off);
+    off += (4 * nblk + 255) & ~(size_t)255;
+    b.block_prefix = reinterpret_cast<int *>(ws + off);
+    return CP_OK;
+}
+
+int launch_binning(const Prepared &P, cudaStream_t stream) {
+    const BinParams &b = P.bp;
+    const int nblk = (int)(((long long)b.nbins + kScanBlock - 1) / kScanBlock);
+    DeviceInfo dev;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    const int clear_blocks = (int)std::min<long long>((b.nbins + 255) / 256, 8LL * dev.sm_count);
+    bin_clear_kernel<<<std::max(clear_blocks, 1), 256, 0, stream>>>(b);
+    if (b.n > 0) bin_count_kernel<<<(b.n + 255) / 256, 256, 0, stream>>>(b);
+    bin_scan_local_kernel<<<nblk, 256, 0, stream>>>(b);
+    bin_scan_blocks_kernel<<<1, 1024, 0, stream>>>(b, nblk);
+    if (b.n > 0) bin_scatter_kernel<<<(b.n + 255) / 256, 256, 0, stream>>>(b);
+    bin_sort_pack_kernel<<<(b.nbins + 7) / 8, 256, 0, stream>>>(b);
+    if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
+    note_launches(b.n > 0 ? 6 : 4);
+    return CP_OK;
+}
+
+template <int K>
+int launch_bricks_k(const Prepared &P, const OffsetList &L, float *V, cudaStream_t stream,
+                    unsigned long long *counts = nullptr) {
+    const Grid &g = P.g;
+    BrickParams p;
+    p.nx = g.nx;
+    p.ny = g.ny;
+    p.nz = g.nz;
+    p.ox = g.ox;
+    p.oy = g.oy;
+    p.oz = g.oz;
+    p.h = g.h;
+    const double c = P.bg.c;
+    p.c2 = (float)(c * c);
+    p.cull2 = (float)(c * c * (1.0 + 1.0e-5));
+    p.gc0 = (float)(15.0 / (8.0 * c));
+    p.gc1 = (float)(-5.0 / (4.0 * c * c * c));
+    p.gc2 = (float)(3.0 / (8.0 * c * c * c * c * c));
+    for (int d = 0; d < 3; ++d) p.nb[d] = P.bg.nb[d];
+    p.m = P.bg.m;
+    p.h64 = (double)g.h;
+    p.b64 = (double)P.bg.b;
+    p.nbr[0] = (g.nx + kBrick - 1) / kBrick;
+    p.nbr[1] = (g.ny + kBrick - 1) / kBrick;
+    p.nbr[2] = (g.nz + kBrick - 1) / kBrick;
+    p.padded = P.bp.padded;
+    p.count = P.bp.count;
+    p.start = P.bp.start;
+    p.csr_atoms = P.bp.csr_atoms;
+    p.V = V;
+    p.counts = counts;
+    p.status = device_status_ptr();
+    if (!p.status) return CP_ERR_CUDA;
+    p.n_runs = L.n_runs;
+    for (int r = 0; r < L.n_runs; ++r) {
+        const unsigned u0 = (unsigned)(uint8_t)L.run[r][0], u1 = (unsigned)(uint8_t)L.run[r][1];
+        const unsigned u2 = (unsigned)(uint8_t)L.run[r][2], u3 = (unsigned)(uint8_t)L.run[r][3];
+        p.runs[r] = (int)(u0 | (u1 << 8) | (u2 << 16) | (u3 << 24));
+    }
+    const long long nbricks = (long long)p.nbr[0] * p.nbr[1] * p.nbr[2];
+    if (nbricks > 0x7fffffffll) return CP_ERR_TOO_LARGE;
+    const bool vec = V && (g.nx % 4 == 0) && aligned(V, 16);
+    if (counts)
+        cutoff_brick_kernel<K, false, true><<<(unsigned)nbricks, kBrickThreads, 0, stream>>>(p);
+    else if (vec)
+        cutoff_brick_kernel<K, true, false><<<(unsigned)nbricks, kBrickThreads, 0, stream>>>(p);
+    else
+        cutoff_brick_kernel<K, false, false><<<(unsigned)nbricks, kBrickThreads, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
+    note_launches(1);
+    return CP_OK;
+}
+
+}  // namespace
+
+}  // namespace cpmap
+
+using namespace cpmap;
+
+extern "C" {
+
+CP_API int cp_bin_atoms(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                        float cutoff, float bin_size, int capacity, void *workspace, size_t workspace_bytes,
+                        void *stream) {
+    Prepared P;
+    int rc = prepare(atoms, n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, workspace, workspace_bytes,
+                     &P);
+    if (rc) return rc;
+    return launch_binning(P, static_cast<cudaStream_t>(stream));
+}
+
+CP_API int cp_cutoff(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff,
+                     float bin_size, int capacity, void *workspace, size_t workspace_bytes, float *V, void *stream) {
+    if (!V) return CP_ERR_INVALID_ARGUMENT;
+    if (!aligned(V, 4)) return CP_ERR_MISALIGNED;
+    Prepared P;
+    int rc = prepare(atoms, n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, workspace, workspace_bytes,
+                     &P);
+    if (rc) return rc;
+    static thread_local OffsetList L;
+    rc = make_offset_list(P.g, P.bg, &L);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = launch_binning(P, s);
+    if (rc) return rc;
+    return capacity == 8 ? launch_bricks_k<8>(P, L, V, s) : launch_bricks_k<16>(P, L, V, s);
+}
+
+CP_API int cp_cutoff_map(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                         float cutoff, float bin_size, int capacity, void *workspace, size_t workspace_bytes, float *V,
+                         void *stream) {
+    if (!V) return CP_ERR_INVALID_ARGUMENT;
+    if (!aligned(V, 4)) return CP_ERR_MISALIGNED;
+    Prepared P;
+    int rc = prepare(atoms, n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, workspace, workspace_bytes,
+                     &P);
+    if (rc) return rc;
+    static thread_local OffsetList L;
+    rc = make_offset_list(P.g, P.bg, &L);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return capacity == 8 ? launch_bricks_k<8>(P, L, V, s) : launch_bricks_k<16>(P, L, V, s);
+}
+
+CP_API int cp_cutoff_pair_counts(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                                  float cutoff, float bin_size, int capacity, void *workspace,
+                                  size_t workspace_bytes, unsigned long long *counts, void *stream) {
+    if (!counts) return CP_ERR_INVALID_ARGUMENT;
+    if (!aligned(counts, 8)) return CP_ERR_MISALIGNED;
+    Prepared P;
+    int rc = prepare(atoms, n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, workspace, workspace_bytes,
+                     &P);
+    if (rc) return rc;
+    static thread_local OffsetList L;
+    rc = make_offset_list(P.g, P.bg, &L);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(counts, 0, 3 * sizeof(unsigned long long), s) != cudaSuccess) return CP_ERR_CUDA;
+    rc = launch_binning(P, s);
+    if (rc) return rc;
+    return capacity == 8 ? launch_bricks_k<8>(P, L, nullptr, s, counts)
+                         : launch_bricks_k<16>(P, L, nullptr, s, counts);
+}
+
+CP_API int cp_cutoff_stats(const void *workspace, size_t workspace_bytes, int n_atoms, int nx, int ny, int nz,
+                           cp_vec3 origin, float h, float cutoff, float bin_size, int capacity,
+                           cp_cutoff_stats_t *out, void *stream) {
+    if (!workspace || !out) return CP_ERR_INVALID_ARGUMENT;
+    cp_cutoff_layout L;
+    int rc = cp_cutoff_layout_of(n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, &L);
+    if (rc) return rc;
+    if (workspace_bytes < L.total_bytes) return CP_ERR_WORKSPACE_TOO_SMALL;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CP_ERR_CUDA;
+    int v[8];
+    if (cudaMemcpy(v, static_cast<const char *>(workspace) + L.off_stats, sizeof(v), cudaMemcpyDeviceToHost) !=
+        cudaSuccess)
+        return CP_ERR_CUDA;
+    out->n_binned = v[0];
+    out->n_dropped = v[1];
+    out->n_overflow = v[2];
+    out->max_bin_count = v[3];
+    return CP_OK;
+}
+
+}  // extern "C"

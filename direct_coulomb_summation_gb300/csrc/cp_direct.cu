@@ -1,0 +1,428 @@
+// cp_direct.cu -- direct Coulomb summation V(g) = sum_a q_a / r on sm_103a.
+//
+// Mapping (PMPP ch.18 notes "Case study -- electrostatic potential map",
+// sections 18.2-18.4, rebuilt for GB300):
+//   * gather: a thread owns grid points and every atom streams past it, so
+//     each thread writes only its own points and no atomics are needed
+//     (section 18.2);
+//   * coarsening: a thread owns a patch of 4 consecutive x points (one
+//     float4 of the x-fastest output) times PY rows in y times PZ planes in z;
+//     per atom the x differences are computed once per patch column and
+//     dy^2 + dz^2 once per row, so a pair costs FFMA (r^2), MUFU (rsqrt) and
+//     FFMA (accumulate) (section 18.3; the pwwt.cn article's section 三 does
+//     the same with 8 points per thread);
+//   * coalescing: neighbouring lanes own neighbouring x quads, so a warp
+//     stores 32 consecutive float4s of a row (section 18.4 and the article's
+//     coarsen-plus-coalesce kernel, section 三);
+//   * atom tiles: instead of 4K-atom chunks in constant memory re-launched
+//     per chunk (section 18.2), one launch streams 512-atom tiles from global
+//     memory into a 3-stage shared-memory ring with 1-D TMA bulk copies; all
+//     threads read the same atom (a shared-memory broadcast);
+//   * accuracy: each tile's contribution is summed in a separate register
+//     and then added to the running total, so the fp32 rounding error grows
+//     like (tile + n_atoms / tile) instead of n_atoms;
+//   * small grids: when there are too few point patches to fill the GPU, S
+//     CTAs of a thread-block cluster share one tile of points and take 1/S
+//     of the atoms each; their partial sums meet in distributed shared
+//     memory and are added in rank order (deterministic, no atomics, no
+//     global scratch).
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "cp_device.cuh"
+#include "cp_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace cpmap {
+
+constexpr int kDirectThreads = 128;
+constexpr int kDirectTile = 512;  // atoms per shared-memory stage (8 KiB)
+constexpr int kDirectStages = 3;
+constexpr int kDirectSmem = kDirectStages * kDirectTile * 16;
+constexpr int kMaxSplit = 8;  // portable cluster size
+
+struct DirectParams {
+    const float4 *atoms;
+    int n_atoms;
+    int split;  // CTAs per cluster sharing one tile of points
+    int nx, ny, nz;
+    float ox, oy, oz, h;
+    int qx;         // x quads per row
+    int yb;         // y blocks of PY rows
+    long long npatch;
+    float *V;
+    unsigned int *status;
+};
+
+// Stores one x quad of row (y, z): a float4 when the row is 16-byte aligned
+// and complete, else the in-range scalars.
+template <bool VEC>
+__device__ __forceinline__ void store_quad(const DirectParams &p, int i0, int y, int z, float4 v) {
+    if (y >= p.ny || z >= p.nz) return;
+    float *row = p.V + ((long long)z * p.ny + y) * p.nx;
+    if (VEC) {
+        *reinterpret_cast<float4 *>(row + i0) = v;
+    } else {
+        if (i0 + 0 < p.nx) row[i0 + 0] = v.x;
+        if (i0 + 1 < p.nx) row[i0 + 1] = v.y;
+        if (i0 + 2 < p.nx) row[i0 + 2] = v.z;
+        if (i0 + 3 < p.nx) row[i0 + 3] = v.w;
+    }
+}
+
+template <int PY, int PZ, bool VEC>
+__global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_constant__ DirectParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ uint64_t full[kDirectStages];
+    float4 *ring = reinterpret_cast<float4 *>(smem);
+
+    const int tid = threadIdx.x;
+    const int split = p.split;
+    const int rank = (int)(blockIdx.x % (unsigned)split);
+    const long long ptile = blockIdx.x / (unsigned)split;
+    const long long patch = ptile * kDirectThreads + tid;
+
+    // This CTA's slice of the atoms.
+    const int a_begin = (int)((long long)p.n_atoms * rank / split);
+    const int a_end = (int)((long long)p.n_atoms * (rank + 1) / split);
+    const int n_local = a_end - a_begin;
+    const int n_tiles = (n_local + kDirectTile - 1) / kDirectTile;
+
+    // This thread's patch: x quad qx, y block yb, z block zb (idle threads past
+    // the last patch compute a copy of it and store nothing).
+    const long long pc = patch < p.npatch ? patch : p.npatch - 1;
+    const int qx = (int)(pc % p.qx);
+    const long long t = pc / p.qx;
+    const int yb = (int)(t % p.yb);
+    const int zb = (int)(t / p.yb);
+    const int i0 = 4 * qx, j0 = PY * yb, k0 = PZ * zb;
+    float x[4], y[PY], z[PZ];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) x[c] = fmaf((float)(i0 + c), p.h, p.ox);
+#pragma unroll
+    for (int j = 0; j < PY; ++j) y[j] = fmaf((float)(j0 + j), p.h, p.oy);
+#pragma unroll
+    for (int k = 0; k < PZ; ++k) z[k] = fmaf((float)(k0 + k), p.h, p.oz);
+
+    if (tid == 0) {
+        for (int s = 0; s < kDirectStages; ++s) mbar_init(&full[s], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    auto issue = [&](int tile, int stage) {
+        const int n = min(kDirectTile, n_local - tile * kDirectTile);
+        const uint32_t bytes = (uint32_t)n * 16u;
+        mbar_arrive_expect_tx(&full[stage], bytes);
+        bulk_g2s(ring + stage * kDirectTile, p.atoms + a_begin + (long long)tile * kDirectTile, bytes, &full[stage]);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < kDirectStages && s < n_tiles; ++s) issue(s, s);
+    }
+
+    float acc[PZ][PY][4];
+#pragma unroll
+    for (int k = 0; k < PZ; ++k)
+#pragma unroll
+        for (int j = 0; j < PY; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[k][j][c] = 0.0f;
+
+    for (int it = 0; it < n_tiles; ++it) {
+        const int stage = it % kDirectStages;
+        mbar_wait(&full[stage], (uint32_t)((it / kDirectStages) & 1), p.status);
+        const float4 *tile = ring + stage * kDirectTile;
+        const int n = min(kDirectTile, n_local - it * kDirectTile);
+
+        float part[PZ][PY][4];
+#pragma unroll
+        for (int k = 0; k < PZ; ++k)
+#pragma unroll
+            for (int j = 0; j < PY; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) part[k][j][c] = 0.0f;
+
+#pragma unroll 2
+        for (int a = 0; a < n; ++a) {
+            const float4 at = tile[a];  // same address in every lane: broadcast
+            float dx[4], dy2[PY];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) dx[c] = x[c] - at.x;
+#pragma unroll
+            for (int j = 0; j < PY; ++j) {
+                const float dy = y[j] - at.y;
+                dy2[j] = dy * dy;
+            }
+#pragma unroll
+            for (int k = 0; k < PZ; ++k) {
+                const float dz = z[k] - at.z;
+#pragma unroll
+                for (int j = 0; j < PY; ++j) {
+                    const float dyz2 = fmaf(dz, dz, dy2[j]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float r2 = fmaf(dx[c], dx[c], dyz2);
+                        part[k][j][c] = fmaf(at.w, sfu_rsqrt(r2), part[k][j][c]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < PZ; ++k)
+#pragma unroll
+            for (int j = 0; j < PY; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[k][j][c] += part[k][j][c];
+
+        __syncthreads();  // every thread is done with this stage
+        if (tid == 0 && it + kDirectStages < n_tiles) issue(it + kDirectStages, stage);
+    }
+
+    if (split == 1) {
+        if (patch < p.npatch) {
+#pragma unroll
+            for (int k = 0; k < PZ; ++k)
+#pragma unroll
+                for (int j = 0; j < PY; ++j)
+                    store_quad<VEC>(p, i0, j0 + j, k0 + k,
+                                    make_float4(acc[k][j][0], acc[k][j][1], acc[k][j][2], acc[k][j][3]));
+        }
+        return;
+    }
+
+    // Cluster reduction: partials in this CTA's shared memory (the ring is
+    // free: the last stage was consumed before the final __syncthreads),
+    // summed over ranks 0..S-1 in order by the CTA that owns each element.
+    constexpr int R = PY * PZ;
+    float4 *partial = ring;  // [R][kDirectThreads] float4
+#pragma unroll
+    for (int k = 0; k < PZ; ++k)
+#pragma unroll
+        for (int j = 0; j < PY; ++j)
+            partial[(k * PY + j) * kDirectThreads + tid] =
+                make_float4(acc[k][j][0], acc[k][j][1], acc[k][j][2], acc[k][j][3]);
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int n_elem = R * kDirectThreads;
+    const int e_begin = n_elem * rank / split;
+    const int e_end = n_elem * (rank + 1) / split;
+    for (int e = e_begin + tid; e < e_end; e += kDirectThreads) {
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < split; ++r) {
+            const float4 v = cluster.map_shared_rank(partial, r)[e];
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        const int row = e / kDirectThreads;
+        const long long pe = ptile * kDirectThreads + (e % kDirectThreads);
+        if (pe < p.npatch) {
+            const int eqx = (int)(pe % p.qx);
+            const long long et = pe / p.qx;
+            const int eyb = (int)(et % p.yb);
+            const int ezb = (int)(et / p.yb);
+            store_quad<VEC>(p, 4 * eqx, PY * eyb + row % PY, PZ * ezb + row / PY, s);
+        }
+    }
+    cluster.sync();  // no CTA leaves while others still read its shared memory
+}
+
+// ---------------------------------------------------------------------------
+// launch planning
+
+namespace {
+
+using KernelFn = void (*)(DirectParams);
+
+struct Variant {
+    int py, pz;
+    KernelFn vec, scalar;
+};
+
+const Variant kVariants[] = {
+    {4, 2, direct_kernel<4, 2, true>, direct_kernel<4, 2, false>},
+    {2, 2, direct_kernel<2, 2, true>, direct_kernel<2, 2, false>},
+    {4, 1, direct_kernel<4, 1, true>, direct_kernel<4, 1, false>},
+    {2, 1, direct_kernel<2, 1, true>, direct_kernel<2, 1, false>},
+    {1, 1, direct_kernel<1, 1, true>, direct_kernel<1, 1, false>},
+};
+constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
+
+// Resident CTAs per GPU for variant v and cluster size s (cached per device).
+std::mutex g_plan_mutex;
+int g_slots[64][kNumVariants][kMaxSplit + 1];
+
+int resident_ctas(int v, int s, bool vec, const DeviceInfo &dev) {
+    std::lock_guard<std::mutex> lock(g_plan_mutex);
+    int &cached = g_slots[dev.device][v][s];
+    if (cached > 0) return cached;
+    KernelFn fn = vec ? kVariants[v].vec : kVariants[v].scalar;
+    int slots = 0;
+    if (s == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDirectThreads, kDirectSmem) != cudaSuccess)
+            return -1;
+        slots = per_sm * dev.sm_count;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(s * 64, 1, 1);
+        cfg.blockDim = dim3(kDirectThreads, 1, 1);
+        cfg.dynamicSmemBytes = kDirectSmem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = s;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) return -1;
+        slots = clusters * s;
+    }
+    cached = slots > 0 ? slots : 1;
+    return cached;
+}
+
+struct Plan {
+    int variant;
+    int split;
+    long long ptiles;
+    int qx, yb;
+    long long npatch;
+};
+
+// Picks the patch shape and cluster split with the smallest modelled time:
+// waves x (points per CTA) x (atoms per CTA), plus a fixed cost per CTA wave.
+int plan_direct(const Grid &g, int n_atoms, bool vec, const DeviceInfo &dev, Plan *out) {
+    double best = INFINITY;
+    for (int v = 0; v < kNumVariants; ++v) {
+        const int py = kVariants[v].py, pz = kVariants[v].pz;
+        if (pz > 1 && g.nz < pz) continue;
+        if (py > 1 && g.ny < py) continue;
+        const long long qx = (g.nx + 3) / 4, yb = (g.ny + py - 1) / py, zb = (g.nz + pz - 1) / pz;
+        const long long npatch = qx * yb * zb;
+        const long long ctas = (npatch + kDirectThreads - 1) / kDirectThreads;
+        const double pts = (double)kDirectThreads * 4 * py * pz;
+        for (int s = 1; s <= kMaxSplit; ++s) {
+            if (s > 1 && (long long)n_atoms < (long long)s * 64) break;
+            if (ctas * s > 0x7fffffffll) break;
+            const int slots = resident_ctas(v, s, vec, dev);
+            if (slots < 0) return CP_ERR_CUDA;
+            const double waves = std::ceil((double)(ctas * s) / slots);
+            const double atoms = std::max(1.0, (double)n_atoms / s);
+            // small patches pay more issue slots per pair (x differences and
+            // row sums are amortised over fewer points)
+            const double issue = 3.0 + (5.0 + 2.0 * py + pz + py * pz) / (4.0 * py * pz);
+            const double t = waves * (pts * atoms * std::max(1.0, issue / 7.0) + 4.0e4);
+            if (t < best * 0.98) {
+                best = t;
+                out->variant = v;
+                out->split = s;
+                out->ptiles = ctas;
+                out->qx = (int)qx;
+                out->yb = (int)yb;
+                out->npatch = npatch;
+            }
+        }
+    }
+    return std::isfinite(best) ? CP_OK : CP_ERR_INVALID_ARGUMENT;
+}
+
+}  // namespace
+
+int launch_direct(const float *atoms, int n_atoms, const Grid &g, float *V, cudaStream_t stream,
+                  int force_variant, int force_split) {
+    DeviceInfo dev;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    const bool vec = (g.nx % 4 == 0) && aligned(V, 16);
+    Plan plan;
+    rc = plan_direct(g, n_atoms, vec, dev, &plan);
+    if (rc) return rc;
+    if (force_variant >= 0 && force_variant < kNumVariants) {
+        const int v = force_variant;
+        const int py = kVariants[v].py, pz = kVariants[v].pz;
+        plan.variant = v;
+        plan.qx = (g.nx + 3) / 4;
+        plan.yb = (g.ny + py - 1) / py;
+        plan.npatch = (long long)plan.qx * plan.yb * ((g.nz + pz - 1) / pz);
+        plan.ptiles = (plan.npatch + kDirectThreads - 1) / kDirectThreads;
+    }
+    if (force_split >= 1 && force_split <= kMaxSplit) plan.split = force_split;
+
+    DirectParams p;
+    p.atoms = reinterpret_cast<const float4 *>(atoms);
+    p.n_atoms = n_atoms;
+    p.split = plan.split;
+    p.nx = g.nx;
+    p.ny = g.ny;
+    p.nz = g.nz;
+    p.ox = g.ox;
+    p.oy = g.oy;
+    p.oz = g.oz;
+    p.h = g.h;
+    p.qx = plan.qx;
+    p.yb = plan.yb;
+    p.npatch = plan.npatch;
+    p.V = V;
+    p.status = device_status_ptr();
+    if (!p.status) return CP_ERR_CUDA;
+
+    KernelFn fn = vec ? kVariants[plan.variant].vec : kVariants[plan.variant].scalar;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(plan.ptiles * plan.split), 1, 1);
+    cfg.blockDim = dim3(kDirectThreads, 1, 1);
+    cfg.dynamicSmemBytes = kDirectSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = plan.split;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = plan.split > 1 ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, fn, p) != cudaSuccess) return CP_ERR_CUDA;
+    note_launches(1);
+    return CP_OK;
+}
+
+}  // namespace cpmap
+
+using namespace cpmap;
+
+extern "C" {
+
+CP_API int cp_direct(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float *V,
+                     void *stream) {
+    Grid g;
+    int rc = check_grid(nx, ny, nz, origin, h, &g);
+    if (rc) return rc;
+    if (n_atoms < 0 || !V || (n_atoms > 0 && !atoms)) return CP_ERR_INVALID_ARGUMENT;
+    if (n_atoms > 0 && !aligned(atoms, 16)) return CP_ERR_MISALIGNED;
+    if (!aligned(V, 4)) return CP_ERR_MISALIGNED;
+    return launch_direct(atoms, n_atoms, g, V, static_cast<cudaStream_t>(stream), -1, 0);
+}
+
+// Same as cp_direct with the patch shape (index into the variant table:
+// 0 = 4x4x2, 1 = 4x2x2, 2 = 4x4x1, 3 = 4x2x1, 4 = 4x1x1 points) and the
+// cluster split forced (pass -1 / 0 to let the planner choose).  For tests
+// and tuning sweeps.
+CP_API int cp_direct_config(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                            float *V, int variant, int split, void *stream) {
+    Grid g;
+    int rc = check_grid(nx, ny, nz, origin, h, &g);
+    if (rc) return rc;
+    if (n_atoms < 0 || !V || (n_atoms > 0 && !atoms)) return CP_ERR_INVALID_ARGUMENT;
+    if (n_atoms > 0 && !aligned(atoms, 16)) return CP_ERR_MISALIGNED;
+    if (!aligned(V, 4)) return CP_ERR_MISALIGNED;
+    if (variant >= kNumVariants || split > kMaxSplit || split < 0) return CP_ERR_INVALID_ARGUMENT;
+    return launch_direct(atoms, n_atoms, g, V, static_cast<cudaStream_t>(stream), variant, split);
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// cp_probe.cu -- microbenchmarks of the SM pipes the potential map runs on:
+// the SFU (MUFU) reciprocal square root and exponential, and the FP32 FMA
+// pipe (scalar and paired f32x2).  They give the per-SM, per-clock
+// throughputs that the roofline of the direct and cutoff kernels is built
+// from.  One CTA per SM (a large shared-memory request keeps a second CTA
+// off the SM); each CTA times itself with clock64, so the rate is per SM
+// clock cycle whatever the clock frequency was.
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "cp_device.cuh"
+#include "cp_internal.h"
+
+namespace cpmap {
+
+constexpr int kProbeChains = 8;
+constexpr int kProbeSmem = 160 * 1024;
+
+template <int KIND>
+__global__ void probe_kernel(int iters, float seed, long long *cycles, float *sink) {
+    float v[kProbeChains];
+#pragma unroll
+    for (int c = 0; c < kProbeChains; ++c) v[c] = seed + 0.001f * (float)(threadIdx.x + c);
+    __syncthreads();
+    long long t0 = 0;
+    if (threadIdx.x == 0) t0 = clock64();
+    __syncthreads();
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int c = 0; c < kProbeChains; ++c) {
+            if (KIND == 0) {
+                v[c] = sfu_rsqrt(v[c]);
+            } else if (KIND == 1) {
+                v[c] = fmaf(v[c], 0.999f, 0.0013f);
+            } else if (KIND == 2) {
+                float y;
+                asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(v[c]));
+                v[c] = y;
+            }
+        }
+        if (KIND == 3) {
+#pragma unroll
+            for (int c = 0; c < kProbeChains; c += 2) {
+                unsigned long long a, r;
+                asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(v[c]), "f"(v[c + 1]));
+                const unsigned long long m = 0x3f7fbe773f7fbe77ull;  // (0.999f, 0.999f)
+                const unsigned long long d = 0x3aaa64c33aaa64c3ull;  // (0.0013f, 0.0013f)
+                asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(m), "l"(d));
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(v[c]), "=f"(v[c + 1]) : "l"(r));
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) cycles[blockIdx.x] = clock64() - t0;
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < kProbeChains; ++c) s += v[c];
+    if (s == 12345.678f) sink[threadIdx.x] = s;  // keeps the chains alive
+}
+
+}  // namespace cpmap
+
+using namespace cpmap;
+
+extern "C" {
+
+CP_API int cp_probe_pipe_rate(int kind, int warps, int iters, double *ops_per_clk, double *ms, void *stream) {
+    if (kind < 0 || kind > 3 || warps < 1 || warps > 32 || iters < 1 || !ops_per_clk) return CP_ERR_INVALID_ARGUMENT;
+    DeviceInfo dev;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    long long *cycles = nullptr;
+    float *sink = nullptr;
+    if (cudaMalloc(&cycles, sizeof(long long) * dev.sm_count) != cudaSuccess) return CP_ERR_CUDA;
+    if (cudaMalloc(&sink, sizeof(float) * 1024) != cudaSuccess) {
+        cudaFree(cycles);
+        return CP_ERR_CUDA;
+    }
+    void (*fns[4])(int, float, long long *, float *) = {probe_kernel<0>, probe_kernel<1>, probe_kernel<2>,
+                                                         probe_kernel<3>};
+    auto fn = fns[kind];
+    rc = CP_OK;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem) != cudaSuccess ||
+        cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        rc = CP_ERR_CUDA;
+    } else {
+        fn<<<dev.sm_count, warps * 32, kProbeSmem, s>>>(16, 0.75f, cycles, sink);  // warm-up
+        cudaEventRecord(e0, s);
+        fn<<<dev.sm_count, warps * 32, kProbeSmem, s>>>(iters, 0.75f, cycles, sink);
+        cudaEventRecord(e1, s);
+        if (cudaStreamSynchronize(s) != cudaSuccess) rc = CP_ERR_CUDA;
+        note_launches(2);
+    }
+    if (rc == CP_OK) {
+        std::vector<long long> cyc(dev.sm_count);
+        float t = 0.f;
+        if (cudaMemcpy(cyc.data(), cycles, sizeof(long long) * dev.sm_count, cudaMemcpyDeviceToHost) != cudaSuccess ||
+            cudaEventElapsedTime(&t, e0, e1) != cudaSuccess) {
+            rc = CP_ERR_CUDA;
+        } else {
+            const double ops = (double)warps * 32.0 * kProbeChains * (double)iters;
+            double sum = 0.0;
+            for (long long c : cyc) sum += ops / (double)(c > 0 ? c : 1);
+            *ops_per_clk = sum / dev.sm_count;
+            if (ms) *ms = t;
+        }
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaFree(cycles);
+    cudaFree(sink);
+    return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,269 @@
+/*
+ * cpmap.h -- C ABI of the GB300 (sm_103a) electrostatic potential-map library
+ * (libcpmap.so).
+ *
+ * What it computes
+ *   The electrostatic potential on a regular 3-D grid,
+ *       V(g) = sum_a q_a / |r_a - g|,
+ *   as defined in the PMPP ch.18 study notes ("Case study -- electrostatic
+ *   potential map", section 18.1; the pwwt.cn chapter-18 article, section 一,
+ *   gives the same sum).  Two routes:
+ *     cp_direct  direct Coulomb summation as a gather: a thread owns grid
+ *                points and atom tiles stream past it, no atomics (notes,
+ *                sections 18.2-18.4).
+ *     cp_cutoff  cutoff summation of the switched term
+ *                    q * (1/r - g(r)),  r < c,
+ *                    g(r) = GC0 + GC1 r^2 + GC2 r^4
+ *                         = (1/c)(15/8 - 5/4 (r/c)^2 + 3/8 (r/c)^4)
+ *                over atoms binned into a uniform cell grid, visiting the
+ *                bins of a precomputed neighbourhood offset list (Input
+ *                Binning lecture, slides "Large Bin Cut-off Kernel Code" (24),
+ *                "Neighborhood Offset List (Pre-calculated)" (27), "Pseudo
+ *                Code of an Implementation" (28), "Details on Small Bin
+ *                Design" (30)).
+ *   There is no Coulomb constant: V is in units of charge / length.
+ *
+ * Conventions shared by every entry point
+ *   atoms      float32 [n_atoms][4] = (x, y, z, q), the 16-byte atom record
+ *              of the notes' section 18.2.  DEVICE pointer, 16-byte aligned.
+ *   grid       nx * ny * nz points; point (i, j, k) sits at
+ *              origin + (i*h, j*h, k*h).  1 <= nx, ny, nz <= 2^24 and
+ *              nx*ny*nz < 2^31.
+ *   V          float32 [nz][ny][nx], x fastest: V[(k*ny + j)*nx + i] (notes,
+ *              section 18.4).  DEVICE pointer, 4-byte aligned (16-byte
+ *              alignment and nx % 4 == 0 enable vector stores).  V is
+ *              OVERWRITTEN, never accumulated into.
+ *   stream     a cudaStream_t passed as void* (NULL = the legacy default
+ *              stream).  Compute calls are asynchronous on that stream; the
+ *              caller keeps every buffer alive until the stream has passed
+ *              the call.
+ *   ownership  the caller allocates and frees every buffer (atoms, V and the
+ *              cutoff workspace).  The library allocates no device memory.
+ *   errors     every int-returning call returns CP_OK (0) or a negative
+ *              cp_status.  Arguments are checked on the host before any
+ *              launch; a rejected call launches nothing and touches no
+ *              buffer.  Problems found on the device (a bounded wait that ran
+ *              out, more atoms than a range allows) are never traps: kernels
+ *              record them in a device status word that cp_device_status()
+ *              reads.
+ *   singular   an atom exactly on a grid point (r = 0) has no defined
+ *              potential there; the value at that point is then inf/nan.
+ */
+#ifndef CPMAP_H
+#define CPMAP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CP_API __attribute__((visibility("default")))
+#else
+#define CP_API
+#endif
+
+/* Return codes. */
+typedef enum {
+    CP_OK = 0,
+    CP_ERR_INVALID_ARGUMENT = -1,  /* null pointer, non-positive size, non-finite value */
+    CP_ERR_MISALIGNED = -2,        /* atoms or workspace not aligned as required */
+    CP_ERR_TOO_LARGE = -3,         /* grid, bin grid or offset list beyond the library's limits */
+    CP_ERR_WORKSPACE_TOO_SMALL = -4,
+    CP_ERR_UNSUPPORTED = -5,       /* e.g. a bin capacity other than 8 or 16 */
+    CP_ERR_CUDA = -6,              /* a CUDA runtime call or launch failed */
+    CP_ERR_DEVICE = -7             /* a kernel reported a problem (see cp_device_status) */
+} cp_status;
+
+/* Device status bits (cp_device_status). */
+#define CP_DEVICE_WAIT_TIMEOUT 0x1u /* a bounded wait on a shared-memory barrier gave up */
+#define CP_DEVICE_RANGE 0x2u        /* an index fell outside a buffer; the access was skipped */
+
+/* A point or vector in Angstrom. */
+typedef struct {
+    float x, y, z;
+} cp_vec3;
+
+/* ------------------------------------------------------------------------ */
+/* Direct Coulomb summation (notes, sections 18.1-18.4).
+ *
+ * V(g) = sum over all n_atoms atoms of q / r for every grid point, computed
+ * in fp32 with rsqrt on the SFU, atom tiles accumulated block-wise.
+ * n_atoms may be 0 (V is then all zero).  Needs no workspace.
+ * Returns CP_OK, CP_ERR_INVALID_ARGUMENT, CP_ERR_MISALIGNED (atoms not
+ * 16-byte aligned), CP_ERR_TOO_LARGE or CP_ERR_CUDA.                        */
+CP_API int cp_direct(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float *V,
+                     void *stream);
+
+/* cp_direct with the per-thread point patch and the cluster split forced,
+ * for tests and tuning sweeps.  variant: -1 = planner's choice, else the
+ * patch of 4 x-points times (PY, PZ) rows/planes with
+ * 0 = (4,2), 1 = (2,2), 2 = (4,1), 3 = (2,1), 4 = (1,1).  split: 0 =
+ * planner's choice, else 1..8 CTAs of a cluster share one tile of points and
+ * take 1/split of the atoms each (their partial sums meet in distributed
+ * shared memory).  Results agree with cp_direct up to fp32 rounding order.
+ * Same errors as cp_direct, plus CP_ERR_INVALID_ARGUMENT for an unknown
+ * variant or split.                                                         */
+CP_API int cp_direct_config(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                            float *V, int variant, int split, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Cutoff summation (Input Binning lecture, slides 24-37).
+ *
+ * Bin geometry (m bins of margin so that every atom within c of the grid is
+ * binned; the bin-grid origin is rounded to fp32 once):
+ *     m    = ceil(c / b)
+ *     bo_d = float(origin_d - m*b)                      (double, rounded once)
+ *     nb_d = ceil(((N_d - 1)*h + 2*m*b) / b) + 1
+ * An atom goes to bin (ux, uy, uz), u_d = floor(float(float(a_d - bo_d) / b))
+ * (two IEEE fp32 roundings, no fused operations), linear index
+ * (uz*nb_y + uy)*nb_x + ux, when every u_d is in [0, nb_d); other atoms
+ * (and atoms with non-finite coordinates) are dropped and counted.
+ *
+ * Within a bin atoms keep ascending input order.  The first `capacity` atoms
+ * of each bin fill its fixed-capacity slots (slide "Coalesced Global Memory
+ * Access to Atom Data" (33)); unused slots hold the pad record
+ * (1e18, 1e18, 1e18, 0).  Atoms past the capacity are the bin's overflow
+ * ("extra atoms", slide "Handling Overfull Bins" (34)); they stay in the
+ * bin-sorted array and are swept on the GPU, not on the CPU.
+ *
+ * A pair contributes iff r^2 < c^2 (strict).  capacity must be 8 (the
+ * lecture's 128-byte bins) or 16 (256-byte bins).                          */
+
+/* Where each array lives inside a cutoff workspace (byte offsets from its
+ * base, each a multiple of 256), for inspection and tests. */
+typedef struct {
+    int nb[3];                 /* bins per axis */
+    float bo[3];               /* bin-grid origin */
+    int margin_bins;           /* m */
+    int capacity;              /* K */
+    long long nbins;           /* nb[0]*nb[1]*nb[2] */
+    size_t off_count;          /* int32 [nbins]        atoms per bin */
+    size_t off_start;          /* int32 [nbins + 1]    exclusive prefix sum of count */
+    size_t off_csr_index;      /* int32 [n_atoms]      input index, sorted by (bin, index) */
+    size_t off_csr_atoms;      /* float32 [n_atoms][4] atoms in that order */
+    size_t off_padded;         /* float32 [nbins][K][4] fixed-capacity slots */
+    size_t off_stats;          /* int32 [8]            see cp_cutoff_stats */
+    size_t off_scratch;        /* internal */
+    size_t total_bytes;        /* workspace size needed */
+} cp_cutoff_layout;
+
+/* Host-only: fills *out for these arguments.  Returns CP_OK,
+ * CP_ERR_INVALID_ARGUMENT, CP_ERR_UNSUPPORTED or CP_ERR_TOO_LARGE. */
+CP_API int cp_cutoff_layout_of(int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff,
+                               float bin_size, int capacity, cp_cutoff_layout *out);
+
+/* Host-only: workspace bytes cp_cutoff / cp_bin_atoms need (0 if the
+ * arguments are invalid). */
+CP_API size_t cp_cutoff_workspace_bytes(int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff,
+                                        float bin_size, int capacity);
+
+/* The whole cutoff map: bin the atoms on the device (count, scan, scatter,
+ * per-bin sort and pack), then one CTA per 8x8x8-point brick sweeps the
+ * neighbourhood offset list's bins and the overflow of those bins, and
+ * writes V.  `workspace` is a DEVICE buffer of at least
+ * cp_cutoff_workspace_bytes(...) bytes, 256-byte aligned, owned by the
+ * caller; its contents on entry do not matter and on return it holds the
+ * bins (see cp_cutoff_layout).  Calls sharing a workspace must not overlap
+ * on the GPU.  Returns CP_OK, CP_ERR_INVALID_ARGUMENT, CP_ERR_MISALIGNED,
+ * CP_ERR_UNSUPPORTED, CP_ERR_TOO_LARGE, CP_ERR_WORKSPACE_TOO_SMALL or
+ * CP_ERR_CUDA.                                                              */
+CP_API int cp_cutoff(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff,
+                     float bin_size, int capacity, void *workspace, size_t workspace_bytes, float *V, void *stream);
+
+/* Only the binning stage of cp_cutoff (same arguments, no V): leaves count,
+ * start, csr_index, csr_atoms, padded and the stats in the workspace. */
+CP_API int cp_bin_atoms(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                        float cutoff, float bin_size, int capacity, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/* Only the map stage of cp_cutoff: the brick kernel and overflow sweep over
+ * bins that a preceding cp_bin_atoms call with the same arguments left in
+ * `workspace` (same stream, or otherwise ordered after it).  Lets a caller
+ * bin once and time the two stages apart.  Same arguments and errors as
+ * cp_cutoff.                                                                */
+CP_API int cp_cutoff_map(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                         float cutoff, float bin_size, int capacity, void *workspace, size_t workspace_bytes, float *V,
+                         void *stream);
+
+/* Work accounting of the cutoff map (no V is written): bins the atoms like
+ * cp_cutoff, then runs the brick traversal in a counting variant that adds
+ * into counts[0..2] (a DEVICE array of 3 uint64, zeroed by the call):
+ *   counts[0]  useful pairs: (grid point, atom) with r^2 < c^2
+ *   counts[1]  pairs evaluated: atoms that passed a warp's sub-box test
+ *              times the warp's 128 points
+ *   counts[2]  pairs examined at bin level: real atoms in the loaded bins
+ *              times the points of the warps that loaded them
+ * counts[0] / counts[2] is the "share of examined atoms within the cutoff"
+ * of slide "Details on Small Bin Design" (30).  Same arguments and errors
+ * as cp_cutoff, with `counts` in place of V.                                */
+CP_API int cp_cutoff_pair_counts(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                                 float cutoff, float bin_size, int capacity, void *workspace, size_t workspace_bytes,
+                                 unsigned long long *counts, void *stream);
+
+/* Counters a binning pass leaves in the workspace. */
+typedef struct {
+    int n_binned;          /* atoms placed in a bin */
+    int n_dropped;         /* atoms outside the bin grid (or non-finite) */
+    int n_overflow;        /* atoms past their bin's capacity */
+    int max_bin_count;     /* most atoms in one bin */
+} cp_cutoff_stats_t;
+
+/* Synchronises `stream`, then copies the counters of the last binning pass
+ * on this workspace to *out.  Returns CP_OK, CP_ERR_INVALID_ARGUMENT or
+ * CP_ERR_CUDA. */
+CP_API int cp_cutoff_stats(const void *workspace, size_t workspace_bytes, int n_atoms, int nx, int ny, int nz,
+                           cp_vec3 origin, float h, float cutoff, float bin_size, int capacity,
+                           cp_cutoff_stats_t *out, void *stream);
+
+/* Host-only: the brick neighbourhood offset list (slide "Neighborhood
+ * Offset List (Pre-calculated)" (27)) as x-runs.  Run r covers the bins
+ * (home_x + dx_lo .. home_x + dx_hi, home_y + dy, home_z + dz) of a brick
+ * whose home bin is `home`; a bin is listed iff its box can come within
+ * c (+ a rounding margin) of some point of some brick (per-axis minimum gap
+ * over all bricks, so one list serves every brick).  runs_out receives
+ * 4 ints per run (dy, dz, dx_lo, dx_hi); pass NULL to query the sizes.
+ * *n_runs and *n_bins receive the list's size.  Returns CP_OK,
+ * CP_ERR_INVALID_ARGUMENT, CP_ERR_TOO_LARGE (list longer than the library
+ * supports) or CP_ERR_WORKSPACE_TOO_SMALL (max_runs too small).            */
+CP_API int cp_offset_list(int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff, float bin_size,
+                          int *runs_out, int max_runs, int *n_runs, int *n_bins);
+
+/* Host-only: the home bin of brick (bx, by, bz) (8x8x8 points each). */
+CP_API int cp_brick_home(int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff, float bin_size, int bx,
+                         int by, int bz, int home_out[3]);
+
+/* ------------------------------------------------------------------------ */
+/* Status and measurement helpers. */
+
+/* Reads and clears the device status word of the current device
+ * (CP_DEVICE_* bits; 0 when every kernel finished cleanly).  Synchronises
+ * `stream` first.  Returns CP_OK or CP_ERR_CUDA. */
+CP_API int cp_device_status(unsigned int *bits_out, void *stream);
+
+/* Number of kernels this library has launched in this process (all
+ * devices), for accounting in benchmarks. */
+CP_API unsigned long long cp_launch_count(void);
+
+/* Static text for a cp_status value. */
+CP_API const char *cp_status_string(int status);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+CP_API int cp_version(void);
+
+/* Microbenchmark of one SM pipe: every SM runs `warps` warps, each thread
+ * issuing `iters` x 8 independent dependent-chain operations of kind
+ * `kind` (0 = MUFU rsqrt.approx.ftz.f32, 1 = FP32 FFMA, 2 = MUFU ex2.approx,
+ * 3 = FP32 FFMA in f32x2 pairs).  Writes the measured throughput in
+ * operations per SM clock cycle (per-SM clock64 cycles, averaged over the
+ * SMs) to *ops_per_clk and the kernel time to *ms.  Synchronous.
+ * Returns CP_OK, CP_ERR_INVALID_ARGUMENT or CP_ERR_CUDA. */
+CP_API int cp_probe_pipe_rate(int kind, int warps, int iters, double *ops_per_clk, double *ms, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPMAP_H */

@@ -1,0 +1,123 @@
+"""GPU parity of the cutoff map (binning + brick kernel + overflow sweep)
+against the fp64 oracle, within |V_gpu - V_ref| <= 2e-4 * sum_{r<c} |q|/r."""
+import numpy as np
+import pytest
+import torch
+
+import direct_coulomb_summation_gb300 as cp
+import oracle
+import workloads
+from gpu_util import assert_within_bound, flat_index, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, c, b, K=16, **kw):
+    V = cp.cutoff(to_dev(w.atoms), w.shape, w.origin, w.h, c, b, capacity=K, **kw)
+    torch.cuda.synchronize()
+    assert cp.device_status() == 0
+    return V
+
+
+@pytest.mark.parametrize("K", [8, 16])
+@pytest.mark.parametrize("seed,n,shape,h,origin,c,b", [
+    (301, 1500, (24, 20, 17), 0.5, (0.0, 0.0, 0.0), 3.0, 1.0),
+    (302, 900, (19, 23, 16), 0.4, (-2.1, 0.7, 3.3), 2.5, 1.3),     # bricks not aligned with bins
+    (303, 2500, (33, 9, 12), 0.5, (1.0, -4.0, 0.5), 4.0, 4.0),     # ragged bricks, big bins
+    (304, 700, (16, 16, 1), 0.5, (0.0, 0.0, 5.0), 2.0, 0.75),      # single plane
+    (305, 3000, (21, 9, 30), 0.3, (10.0, -5.0, 0.25), 1.9, 0.55),
+])
+def test_cutoff_small_full_grid(K, seed, n, shape, h, origin, c, b):
+    w = workloads.random_case(seed, n, shape, h=h, origin=origin, margin=c + 1.0)
+    V = _run(w, c, b, K)
+    ref, bound = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, c)
+    assert_within_bound(V.cpu().numpy(), ref, bound, w.name)
+
+
+@pytest.mark.parametrize("K", [8, 16])
+def test_cutoff_all_atoms_in_one_bin(K):
+    """Every atom in one bin: capacity overflow for every atom past K."""
+    rng = np.random.default_rng(5)
+    shape, h, c, b = (24, 24, 24), 0.5, 3.0, 1.0
+    n = 600
+    atoms = np.empty((n, 4), dtype=np.float32)
+    atoms[:, :3] = (6.0 + rng.uniform(0.05, 0.45, size=(n, 3))).astype(np.float32)
+    atoms[:, 3] = rng.uniform(-1, 1, size=n).astype(np.float32)
+    w = workloads.Workload("one_bin", atoms, shape, (0.0, 0.0, 0.0), h)
+    V = _run(w, c, b, K)
+    ref, bound = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, c)
+    assert_within_bound(V.cpu().numpy(), ref, bound, "one bin")
+
+
+def test_cutoff_atoms_outside_and_nonfinite():
+    w = workloads.random_case(7, 800, (16, 16, 16), margin=12.0)  # many atoms far outside
+    extra = np.array([[np.nan, 1, 1, 1], [np.inf, 1, 1, 1], [1e30, 0, 0, 1]], dtype=np.float32)
+    atoms = np.concatenate([w.atoms, extra])
+    c, b = 2.5, 1.0
+    V = cp.cutoff(to_dev(atoms), w.shape, w.origin, w.h, c, b)
+    torch.cuda.synchronize()
+    ref, bound = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, c)
+    assert_within_bound(V.cpu().numpy(), ref, bound, "outside")
+
+
+def test_cutoff_zero_atoms():
+    V = cp.cutoff(torch.zeros((0, 4), dtype=torch.float32, device="cuda"), (9, 9, 9), (0, 0, 0), 0.5, 2.0, 1.0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(V).item() == 0
+
+
+def test_cutoff_large_c_tends_to_direct():
+    """With every pair inside the cutoff, cutoff + (15/(8c)) sum q = direct + O(r^2/c^3)."""
+    w = workloads.random_case(8, 1200, (20, 16, 12), margin=1.0)
+    c = 200.0
+    Vc = _run(w, c, 64.0)
+    Vd = cp.direct(to_dev(w.atoms), w.shape, w.origin, w.h)
+    torch.cuda.synchronize()
+    qsum = float(w.atoms[:, 3].astype(np.float64).sum())
+    _, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+    diff = (Vc.double() + 15.0 / (8.0 * c) * qsum - Vd.double()).cpu().numpy().reshape(-1)
+    rmax = 30.0
+    lim = (5 / 4) * rmax**2 / c**3 * np.abs(w.atoms[:, 3]).sum() + 4e-4 * bound
+    assert np.all(np.abs(diff) <= lim)
+
+
+def test_cutoff_workspace_reuse_and_determinism():
+    w = workloads.random_case(9, 4000, (40, 32, 24), margin=3.0)
+    c, b = 3.0, 1.0
+    need = cp.cutoff_workspace_bytes(4000, w.shape, w.origin, w.h, c, b)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    a = to_dev(w.atoms)
+    v1 = cp.cutoff(a, w.shape, w.origin, w.h, c, b, workspace=ws).clone()
+    v2 = cp.cutoff(a, w.shape, w.origin, w.h, c, b, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(v1, v2)
+
+
+def test_cutoff_host_buffers_match_device():
+    w = workloads.random_case(10, 900, (20, 12, 6), margin=1.0)
+    vh = cp.cutoff(w.atoms, w.shape, w.origin, w.h, 2.0, 1.0)
+    vd = cp.cutoff(to_dev(w.atoms), w.shape, w.origin, w.h, 2.0, 1.0)
+    torch.cuda.synchronize()
+    assert not vh.is_cuda and torch.equal(vh, vd.cpu())
+
+
+def test_cutoff_uniform_workload_sampled():
+    """100 000 atoms, 200^3 grid, c = 12 A, 4 A bins: full map on the GPU,
+    4096 seeded points by the brute-force oracle."""
+    w = workloads.make("cutoff_uniform")
+    V = _run(w, w.cutoff, w.bin_size)
+    pts = workloads.sample_points(w.shape, 4096, seed=4097)
+    ref, bound = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, w.cutoff, points=pts)
+    got = V.reshape(-1)[torch.from_numpy(flat_index(w.shape, pts)).cuda()].cpu().numpy()
+    assert_within_bound(got, ref, bound, w.name)
+
+
+def test_cutoff_large_workload_sampled():
+    """800 000 atoms (30 % in Gaussian clusters), 400^3 grid: 4096 seeded points
+    by the binned oracle (bit-identical to brute force by its pins)."""
+    w = workloads.make("cutoff_large")
+    V = _run(w, w.cutoff, w.bin_size)
+    pts = workloads.sample_points(w.shape, 4096, seed=4098)
+    ref, bound = oracle.cutoff_binned(w.atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, points=pts)
+    got = V.reshape(-1)[torch.from_numpy(flat_index(w.shape, pts)).cuda()].cpu().numpy()
+    assert_within_bound(got, ref, bound, w.name)

@@ -1,0 +1,124 @@
+"""GPU parity of the direct sum: the sm_103a kernel (through the C ABI)
+against the fp64 oracle, element by element, within
+|V_gpu - V_ref| <= 2e-4 * sum_a |q_a| / r  at every checked point."""
+import numpy as np
+import pytest
+import torch
+
+import direct_coulomb_summation_gb300 as cp
+import oracle
+import workloads
+from gpu_util import assert_within_bound, flat_index, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_full(w, **kw):
+    V = cp.direct(to_dev(w.atoms), w.shape, w.origin, w.h, **kw)
+    torch.cuda.synchronize()
+    assert V.shape == (w.shape[2], w.shape[1], w.shape[0])
+    ref, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+    return assert_within_bound(V.cpu().numpy(), ref, bound, w.name)
+
+
+@pytest.mark.parametrize("seed,n,shape,h,origin", [
+    (101, 1100, (37, 21, 9), 0.37, (-3.25, 1.5, -2.0)),    # 3 atom tiles, ragged x, odd y and z
+    (102, 513, (40, 12, 4), 0.5, (0.0, 0.0, 0.0)),          # one atom past a tile
+    (103, 64, (5, 3, 2), 0.5, (1.0, 1.0, 1.0)),             # tiny grid
+    (104, 2000, (128, 8, 3), 0.25, (-8.0, 0.0, 0.0)),
+    (105, 1, (16, 16, 16), 0.5, (0.0, 0.0, 0.0)),           # single atom
+    (106, 3000, (100, 100, 1), 0.5, (0.0, 0.0, 5.0)),       # plane
+])
+def test_direct_small_full_grid(seed, n, shape, h, origin):
+    w = workloads.random_case(seed, n, shape, h=h, origin=origin, margin=2.0)
+    _check_full(w)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("split", [1, 2, 3, 5, 8])
+def test_direct_every_variant_and_split(variant, split):
+    w = workloads.random_case(200 + variant, 1537, (44, 13, 6), h=0.5, origin=(-1.0, 0.0, 2.0), margin=1.0)
+    _check_full(w, variant=variant, split=split)
+
+
+def test_direct_zero_atoms():
+    w = workloads.random_case(1, 0, (12, 5, 3))
+    V = cp.direct(torch.zeros((0, 4), dtype=torch.float32, device="cuda"), w.shape, w.origin, w.h)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(V).item() == 0
+
+
+def test_direct_unaligned_output_and_odd_nx():
+    w = workloads.random_case(7, 700, (13, 7, 5), h=0.5, margin=1.0)
+    buf = torch.full((13 * 7 * 5 + 1,), float("nan"), device="cuda")
+    out = buf[1:]  # 4-byte aligned only: scalar stores
+    cp.direct(to_dev(w.atoms), w.shape, w.origin, w.h, out=out)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[0]).item()
+    ref, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+    assert_within_bound(out.cpu().numpy(), ref, bound)
+
+
+def test_direct_overwrites_output():
+    w = workloads.random_case(8, 300, (16, 8, 4), margin=1.0)
+    out = torch.full((4, 8, 16), 1e30, device="cuda")
+    cp.direct(to_dev(w.atoms), w.shape, w.origin, w.h, out=out)
+    torch.cuda.synchronize()
+    ref, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+    assert_within_bound(out.cpu().numpy(), ref, bound)
+
+
+def test_direct_deterministic_and_status_clean():
+    w = workloads.random_case(9, 5000, (64, 32, 8), margin=2.0)
+    a = to_dev(w.atoms)
+    v1 = cp.direct(a, w.shape, w.origin, w.h).clone()
+    v2 = cp.direct(a, w.shape, w.origin, w.h)
+    torch.cuda.synchronize()
+    assert torch.equal(v1, v2)
+    assert cp.device_status() == 0
+
+
+def test_direct_host_buffers_match_device():
+    w = workloads.random_case(10, 900, (20, 12, 6), margin=1.0)
+    v_host = cp.direct(w.atoms, w.shape, w.origin, w.h)  # numpy in, CPU tensor out
+    v_dev = cp.direct(to_dev(w.atoms), w.shape, w.origin, w.h)
+    torch.cuda.synchronize()
+    assert not v_host.is_cuda
+    assert torch.equal(v_host, v_dev.cpu())
+
+
+def test_direct_plane_workload_full():
+    """10 000 atoms, the 100x100 plane z-index 10 of a 100x100x50 grid: every point."""
+    w = workloads.make("direct_plane")
+    _check_full(w)
+
+
+@pytest.mark.parametrize("name", ["direct_3d", "direct_protein"])
+def test_direct_workload_sampled(name):
+    """Full-size grid in the launch configuration the benchmark uses; the
+    oracle checks 4096 seeded points."""
+    w = workloads.make(name)
+    V = cp.direct(to_dev(w.atoms), w.shape, w.origin, w.h)
+    torch.cuda.synchronize()
+    pts = workloads.sample_points(w.shape, 4096, seed=4096)
+    ref, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h, points=pts)
+    got = V.reshape(-1)[torch.from_numpy(flat_index(w.shape, pts)).cuda()].cpu().numpy()
+    assert_within_bound(got, ref, bound, name)
+    assert cp.device_status() == 0
+
+
+def test_direct_superposition_on_gpu():
+    """V(A u B) = V(A) + V(B) and V(-q) = -V(q) hold for the GPU map too (within fp32)."""
+    w = workloads.random_case(11, 2048, (32, 16, 8), margin=1.0)
+    a = to_dev(w.atoms)
+    vab = cp.direct(a, w.shape, w.origin, w.h).double()
+    va = cp.direct(a[:1000].contiguous(), w.shape, w.origin, w.h).double()
+    vb = cp.direct(a[1000:].contiguous(), w.shape, w.origin, w.h).double()
+    neg = a.clone()
+    neg[:, 3] = -neg[:, 3]
+    vn = cp.direct(neg, w.shape, w.origin, w.h)
+    torch.cuda.synchronize()
+    _, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+    bound = torch.from_numpy(bound).cuda().reshape(vab.shape)
+    assert torch.all((vab - va - vb).abs() <= 2e-4 * bound)
+    assert torch.equal(vn, -vab.float())  # exact: each term negates
