@@ -284,6 +284,24 @@ def traffic_from_profile(kernel: str, source: str):
     return rec.get("dram_bytes_per_launch")
 
 
+def e2e_times(cp, wd, wc, Vd, Vc, ws, host_atoms_d, host_out_d, host_atoms_c, host_out_c, n):
+    """Seconds per call of the public API with host buffers: pinned atoms in,
+    host V out, copies and synchronisation included (one untimed call first)."""
+    cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
+    t_d = (time.perf_counter() - t0) / n
+    cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY, workspace=ws, out=Vc,
+              host_out=host_out_c)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY, workspace=ws, out=Vc,
+                  host_out=host_out_c)
+    t_c = (time.perf_counter() - t0) / n
+    return t_d, t_c
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -337,15 +355,22 @@ def run_ours(args):
     r_mufu, _ = cp.probe_pipe_rate("mufu_rsqrt", 32, 4096)
     r_ffma, _ = cp.probe_pipe_rate("ffma", 32, 4096)
     # cutoff work accounting (not timed)
-    counts = cp.cutoff_pair_counts(ac, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY, workspace=ws)
+    counts = {"useful": 0, "evaluated": 0, "examined": 0}
+    if args.only in ("both", "cutoff"):
+        counts = cp.cutoff_pair_counts(ac, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY,
+                                       workspace=ws)
 
     sampler = ClockSampler(gpu_id_for(torch, device))
+    do_direct = args.only in ("both", "direct")
+    do_cutoff = args.only in ("both", "cutoff")
     for _ in range(args.warmup):
         flush.fill_(1)
-        run_direct()
+        if do_direct:
+            run_direct()
         flush.fill_(2)
-        run_bin()
-        run_map()
+        if do_cutoff:
+            run_bin()
+            run_map()
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     launches0 = lib.cp_launch_count()
@@ -357,13 +382,16 @@ def run_ours(args):
         e = ev[k]
         flush.fill_(k & 0x7F)
         e[0].record(stream)
-        run_direct()
+        if do_direct:
+            run_direct()
         e[1].record(stream)
         flush.fill_((k + 64) & 0x7F)
         e[2].record(stream)
-        run_bin()
+        if do_cutoff:
+            run_bin()
         e[3].record(stream)
-        run_map()
+        if do_cutoff:
+            run_map()
         e[4].record(stream)
     torch.cuda.synchronize()
     barrier(device)
@@ -379,6 +407,7 @@ def run_ours(args):
     t_bin = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
     t_map = sum(e[3].elapsed_time(e[4]) for e in ev) / 1e3
     t_direct, t_bin, t_map, t_wall = max_over_ranks([t_direct, t_bin, t_map, t_wall], device)
+    t_direct, t_bin, t_map = (max(t, 1e-12) for t in (t_direct, t_bin, t_map))
     K = args.steps
     direct_pairs = float(wd.n_pairs) * world * K
     direct_rate = direct_pairs / t_direct
@@ -416,19 +445,11 @@ def run_ours(args):
     host_atoms_c = torch.from_numpy(wc.atoms).pin_memory()
     host_out_c = torch.empty(Vc.shape, dtype=torch.float32, pin_memory=True)
     n_e2e = max(3, min(K, 10))
-    cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
-    t0 = time.perf_counter()
-    for _ in range(n_e2e):
-        cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
-    t_e2e_d = (time.perf_counter() - t0) / n_e2e
-    cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY, workspace=ws, out=Vc,
-              host_out=host_out_c)
-    t0 = time.perf_counter()
-    for _ in range(n_e2e):
-        cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY, workspace=ws, out=Vc,
-                  host_out=host_out_c)
-    t_e2e_c = (time.perf_counter() - t0) / n_e2e
-    t_e2e_d, t_e2e_c = max_over_ranks([t_e2e_d, t_e2e_c], device)
+    t_e2e_d = t_e2e_c = float("nan")
+    if not args.no_e2e:
+        t_e2e_d, t_e2e_c = e2e_times(cp, wd, wc, Vd, Vc, ws, host_atoms_d, host_out_d, host_atoms_c, host_out_c,
+                                     n_e2e)
+        t_e2e_d, t_e2e_c = max_over_ranks([t_e2e_d, t_e2e_c], device)
 
     if rank != 0:
         if world > 1:
@@ -491,7 +512,7 @@ def run_ours(args):
                 "bound": "alu", "kernel": "cutoff_brick_kernel (cp_cutoff_map)",
                 "achieved": useful_rate, "peak": peak_useful, "unit": "useful pair evals/s",
                 "frac": useful_rate / peak_useful,
-                "time_vs_useful_pair_roofline": peak_useful / useful_rate,
+                "time_vs_useful_pair_roofline": peak_useful / useful_rate if useful_rate > 0 else None,
                 "peak_basis": f"{n_sm} SMs x {per_sm_useful:.2f} useful pairs/clk/SM x {f_mhz:.0f} MHz",
             },
             "roofline_binning": {
@@ -516,6 +537,13 @@ def run_ours(args):
         "wall_ms_per_step": 1e3 * t_wall / K,
         "device": props.name,
     }
+    if not do_cutoff:
+        line["cutoff"] = None
+    if not do_direct:
+        for key in ("value", "roofline", "direct"):
+            line[key] = None
+    if args.no_e2e:
+        line["e2e"] = None
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -525,11 +553,14 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=["both", "direct", "cutoff"], default="both",
+                    help="time one leg only (for profiling; the JSON line then covers that leg)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
