@@ -60,6 +60,7 @@ SIGNATURES = {
     "cp_cutoff_map": (_I, [_P, _I, *_GRID, _F, _F, _I, _P, _SZ, _P, _P]),
     "cp_launch_count": (ctypes.c_ulonglong, []),
     "cp_cutoff_pair_counts": (_I, [_P, _I, *_GRID, _F, _F, _I, _P, _SZ, _P, _P]),
+    "cp_cutoff_no_alloc": (_I, [_P, _I, *_GRID, _F, _F, _I, _P, _P]),
     "cp_cutoff_stats": (_I, [_P, _SZ, _I, *_GRID, _F, _F, _I, ctypes.POINTER(cp_cutoff_stats_t), _P]),
     "cp_offset_list": (_I, [*_GRID, _F, _F, _P, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "cp_brick_home": (_I, [*_GRID, _F, _F, _I, _I, _I, _I * 3]),

@@ -32,6 +32,7 @@
 #include <climits>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "cp_device.cuh"
 #include "cp_internal.h"
@@ -650,6 +651,78 @@ CP_API int cp_cutoff_stats(const void *workspace, size_t workspace_bytes, int n_
     out->n_overflow = v[2];
     out->max_bin_count = v[3];
     return CP_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free cutoff map.
+//
+// Some callers cannot hand the library a workspace: a host program whose
+// device memory is wholly owned by another allocator (a framework's caching
+// pool that has already reserved the device), or code that must not
+// allocate once it is running (a fixed memory budget set at start-up, a
+// plugin that may only use what its host gave it).  For them the cutoff
+// map's scratch lives in a fixed array of this library's module, created
+// when the module is loaded on a device and kept until the process exits.
+// The caller passes only the atoms and V.
+
+namespace cpmap {
+namespace {
+
+constexpr size_t kStaticWorkspaceBytes = size_t(16) << 20;  // 16 MiB per device
+
+// The scratch itself.  In host code this name is only a stand-in for the
+// symbol, never a device address: kernels get the address that
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+std::mutex g_static_ws_mutex;
+void *g_static_ws_ptr[64];
+
+// Device address of g_static_workspace on the current device, looked up
+// once per device (the first call on each device does it).
+void *static_workspace_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+    if (!g_static_ws_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return nullptr;
+        g_static_ws_ptr[dev] = p;
+    }
+    return g_static_ws_ptr[dev];
+}
+
+}  // namespace
+}  // namespace cpmap
+
+extern "C" {
+
+CP_API int cp_cutoff_no_alloc(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                              float cutoff, float bin_size, int capacity, float *V, void *stream) {
+    if (!V) return CP_ERR_INVALID_ARGUMENT;
+    if (!aligned(V, 4)) return CP_ERR_MISALIGNED;
+    cp_cutoff_layout L;
+    int rc = cp_cutoff_layout_of(n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, &L);
+    if (rc) return rc;
+    if (L.total_bytes > kStaticWorkspaceBytes) return CP_ERR_TOO_LARGE;  // beyond the fixed 16 MiB
+    void *ws = static_workspace_ptr();
+    if (!ws) return CP_ERR_CUDA;
+    // Every call reuses the same array and finds the previous call's bins in
+    // it.  Nothing carries over: the binning stage zeroes the per-bin counters
+    // and the counters block before counting, and every other array is
+    // rewritten in full before it is read.
+    Prepared P;
+    rc = prepare(atoms, n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, ws, kStaticWorkspaceBytes, &P);
+    if (rc) return rc;
+    static thread_local OffsetList OL;
+    rc = make_offset_list(P.g, P.bg, &OL);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = launch_binning(P, s);
+    if (rc) return rc;
+    return capacity == 8 ? launch_bricks_k<8>(P, OL, V, s) : launch_bricks_k<16>(P, OL, V, s);
 }
 
 }  // extern "C"

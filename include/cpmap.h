@@ -203,6 +203,35 @@ CP_API int cp_cutoff_pair_counts(const float *atoms, int n_atoms, int nx, int ny
                                  float cutoff, float bin_size, int capacity, void *workspace, size_t workspace_bytes,
                                  unsigned long long *counts, void *stream);
 
+/* The cutoff map with no workspace argument and no allocation, for callers
+ * that cannot allocate device memory themselves: a program whose device
+ * memory is wholly owned by another allocator, or code that may not
+ * allocate once it is running (a fixed budget set at start-up, a plugin
+ * limited to what its host hands it).  The pages have no counterpart; this
+ * is an addition for such callers.
+ *
+ * The scratch that cp_cutoff takes as `workspace` is here a fixed 16 MiB
+ * array inside the library, created on every device that loads the library
+ * and held until the process exits.  Maps whose workspace
+ * (cp_cutoff_workspace_bytes) exceeds 16 MiB are rejected with
+ * CP_ERR_TOO_LARGE before anything runs; 100,000 atoms on a 200^3 grid at
+ * c = 12, b = 4, capacity 16 need about 12 MiB.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture.  The
+ * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
+ *
+ * All calls on a device share the one array and find the previous call's
+ * bins in it; the binning stage clears what must start at zero, so no
+ * result depends on an earlier call.  Calls that overlap on the GPU (on
+ * different streams, or from different threads without ordering) race on
+ * the array: order them, e.g. by issuing them on one stream.
+ *
+ * Arguments, results and the other errors are those of cp_cutoff, without
+ * workspace and workspace_bytes.                                            */
+CP_API int cp_cutoff_no_alloc(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                              float cutoff, float bin_size, int capacity, float *V, void *stream);
+
 /* Counters a binning pass leaves in the workspace. */
 typedef struct {
     int n_binned;          /* atoms placed in a bin */
