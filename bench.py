@@ -38,7 +38,7 @@ import numpy as np  # noqa: E402
 METRIC = "pair evals/s (direct Coulomb) and grid points/s at 12 Å cutoff, % of roofline"
 DIRECT_WL = "direct_3d"
 CUTOFF_WL = "cutoff_uniform"
-CAPACITY = 16
+CAPACITY_DEFAULT = 0
 FLUSH_BYTES = 256 << 20
 
 
@@ -49,7 +49,7 @@ def env_rank():
     return rank, world, local
 
 
-def config_dict(wd, wc):
+def config_dict(wd, wc, capacity):
     return {
         "workload": f"direct {wd.shape[0]}x{wd.shape[1]}x{wd.shape[2]} grid, {wd.n_atoms} atoms, h={wd.h} A; "
         f"cutoff {wc.shape[0]}x{wc.shape[1]}x{wc.shape[2]} grid, {wc.n_atoms} atoms, c={wc.cutoff} A, "
@@ -57,7 +57,7 @@ def config_dict(wd, wc):
         "direct": {"grid": list(wd.shape), "atoms": wd.n_atoms, "h": wd.h, "pairs": wd.n_pairs,
                    "description": wd.description},
         "cutoff": {"grid": list(wc.shape), "atoms": wc.n_atoms, "h": wc.h, "cutoff": wc.cutoff,
-                   "bin_size": wc.bin_size, "capacity": CAPACITY, "brick": [8, 8, 8],
+                   "bin_size": wc.bin_size, "capacity": capacity, "brick": [8, 8, 8],
                    "description": wc.description},
         "l2": "flushed before every timed launch (256 MiB write)",
         "parallelism": "one independent copy per rank (weak scaling)",
@@ -255,7 +255,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": config_dict(wd, wc),
+        "config": config_dict(wd, wc, args.capacity),
         "cpu_baseline": {"value": value, "unit": "pair evals/s", "cores": threads, "kind": "oracle",
                          "sample": f"direct sum at {n_pts} seeded grid points of the {wd.shape} grid x "
                                    f"{wd.n_atoms} atoms per step"},
@@ -284,7 +284,7 @@ def traffic_from_profile(kernel: str, source: str):
     return rec.get("dram_bytes_per_launch")
 
 
-def e2e_times(cp, wd, wc, Vd, Vc, ws, host_atoms_d, host_out_d, host_atoms_c, host_out_c, n):
+def e2e_times(cp, wd, wc, Vd, Vc, ws, host_atoms_d, host_out_d, host_atoms_c, host_out_c, n, capacity):
     """Seconds per call of the public API with host buffers: pinned atoms in,
     host V out, copies and synchronisation included (one untimed call first)."""
     cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
@@ -292,11 +292,11 @@ def e2e_times(cp, wd, wc, Vd, Vc, ws, host_atoms_d, host_out_d, host_atoms_c, ho
     for _ in range(n):
         cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
     t_d = (time.perf_counter() - t0) / n
-    cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY, workspace=ws, out=Vc,
+    cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, capacity, workspace=ws, out=Vc,
               host_out=host_out_c)
     t0 = time.perf_counter()
     for _ in range(n):
-        cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY, workspace=ws, out=Vc,
+        cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, capacity, workspace=ws, out=Vc,
                   host_out=host_out_c)
     t_c = (time.perf_counter() - t0) / n
     return t_d, t_c
@@ -330,12 +330,12 @@ def run_ours(args):
     Vd = torch.empty((wd.shape[2], wd.shape[1], wd.shape[0]), dtype=torch.float32, device=device)
     ac = torch.from_numpy(wc.atoms).to(device)
     Vc = torch.empty((wc.shape[2], wc.shape[1], wc.shape[0]), dtype=torch.float32, device=device)
-    ws_bytes = cp.cutoff_workspace_bytes(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY)
+    ws_bytes = cp.cutoff_workspace_bytes(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     gd = cp._grid(wd.shape, wd.origin, wd.h)
     gc = cp._grid(wc.shape, wc.origin, wc.h)
-    cut = [float(np.float32(wc.cutoff)), float(np.float32(wc.bin_size)), CAPACITY]
+    cut = [float(np.float32(wc.cutoff)), float(np.float32(wc.bin_size)), args.capacity]
 
     def call(rc, where):
         if rc != 0:
@@ -357,7 +357,7 @@ def run_ours(args):
     # cutoff work accounting (not timed)
     counts = {"useful": 0, "evaluated": 0, "examined": 0}
     if args.only in ("both", "cutoff"):
-        counts = cp.cutoff_pair_counts(ac, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY,
+        counts = cp.cutoff_pair_counts(ac, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity,
                                        workspace=ws)
 
     sampler = ClockSampler(gpu_id_for(torch, device))
@@ -428,8 +428,8 @@ def run_ours(args):
     peak_useful = per_sm_useful * n_sm * f_mhz * 1e6 * world
     # binning: HBM bytes it must move at least (atoms in, bin-sorted atoms and
     # indices out, counts and starts, fixed-capacity slots out)
-    L = cp.cutoff_layout(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, CAPACITY)
-    bin_bytes = 16 * wc.n_atoms * 2 + 4 * wc.n_atoms + 8 * int(L.nbins) + 16 * CAPACITY * int(L.nbins)
+    L = cp.cutoff_layout(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity)
+    bin_bytes = 16 * wc.n_atoms * 2 + 4 * wc.n_atoms + 8 * int(L.nbins) + 16 * args.capacity * int(L.nbins)
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -448,7 +448,7 @@ def run_ours(args):
     t_e2e_d = t_e2e_c = float("nan")
     if not args.no_e2e:
         t_e2e_d, t_e2e_c = e2e_times(cp, wd, wc, Vd, Vc, ws, host_atoms_d, host_out_d, host_atoms_c, host_out_c,
-                                     n_e2e)
+                                     n_e2e, args.capacity)
         t_e2e_d, t_e2e_c = max_over_ranks([t_e2e_d, t_e2e_c], device)
 
     if rank != 0:
@@ -482,7 +482,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": config_dict(wd, wc),
+        "config": config_dict(wd, wc, args.capacity),
         "roofline": {
             "bound": "alu",
             "kernel": "direct_kernel (cp_direct)",
@@ -561,6 +561,8 @@ def main(argv=None):
     ap.add_argument("--only", choices=["both", "direct", "cutoff"], default="both",
                     help="time one leg only (for profiling; the JSON line then covers that leg)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--capacity", type=int, choices=[0, 8, 16], default=CAPACITY_DEFAULT,
+                    help="bin capacity of the cutoff leg (0 = contiguous bin-sorted runs, no fixed slots)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

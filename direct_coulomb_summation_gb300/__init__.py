@@ -37,14 +37,17 @@ __all__ = [
     "brick_home",
     "device_status",
     "probe_pipe_rate",
+    "eval_rsqrt",
     "status_string",
     "version",
     "library",
     "DIRECT_VARIANTS",
 ]
 
-# index -> (PY, PZ): per-thread patch of 4 x-points times PY rows times PZ planes
-DIRECT_VARIANTS = {0: (4, 2), 1: (2, 2), 2: (4, 1), 3: (2, 1), 4: (1, 1)}
+# index -> (PY, PZ, EMU): per-thread patch of 4 x-points times PY rows times PZ
+# planes; the first EMU of its 2*PY*PZ point pairs take rsqrt on the FMA pipe
+DIRECT_VARIANTS = {0: (4, 2, 0), 1: (2, 2, 0), 2: (4, 1, 0), 3: (2, 1, 0), 4: (1, 1, 0),
+                   5: (4, 2, 4), 6: (4, 2, 5), 7: (2, 2, 2), 8: (4, 1, 2), 9: (2, 1, 1)}
 
 
 class CpError(RuntimeError):
@@ -265,6 +268,17 @@ def device_status(stream=None) -> int:
 
 
 PIPE_KINDS = {"mufu_rsqrt": 0, "ffma": 1, "mufu_ex2": 2, "ffma2": 3}
+
+
+def eval_rsqrt(x: "torch.Tensor", kind: str = "sfu", stream=None) -> "torch.Tensor":
+    """rsqrt of a float32 CUDA tensor by the kernels' SFU ("sfu") or FMA-pipe ("fma") route."""
+    if not (x.is_cuda and x.dtype == torch.float32):
+        raise ValueError("x must be a float32 CUDA tensor")
+    x = x.contiguous()
+    y = torch.empty_like(x)
+    rc = library().cp_eval_rsqrt({"sfu": 0, "fma": 1}[kind], x.data_ptr(), y.data_ptr(), x.numel(), _stream(stream))
+    _check(rc, "cp_eval_rsqrt")
+    return y
 
 
 def probe_pipe_rate(kind: str, warps: int = 32, iters: int = 4096, stream=None):

@@ -67,6 +67,7 @@ SIGNATURES = {
     "cp_device_status": (_I, [ctypes.POINTER(ctypes.c_uint), _P]),
     "cp_status_string": (ctypes.c_char_p, [_I]),
     "cp_version": (_I, []),
+    "cp_eval_rsqrt": (_I, [_I, _P, _P, _I, _P]),
     "cp_probe_pipe_rate": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _P]),
 }
 

@@ -251,15 +251,27 @@ struct BrickParams {
     int runs[kMaxRuns];  // packed int8 (dy, dz, dx_lo, dx_hi)
 };
 
+// One listed atom with each component duplicated and the coordinates
+// negated: (-x,-x), (-y,-y), (-z,-z), (q,q), so that point - atom is one
+// f32x2 add.
+struct __align__(16) AtomPair {
+    float2 x, y, z, q;
+};
+
 __device__ __forceinline__ int brick_home_dev(int brick, int m, double h, double b) {
     const double t = __dmul_rn(8.0 * (double)brick, h);
     return m + (int)floor(__ddiv_rn(t, b));
 }
 
+// Atoms per shared-memory stage.  The producer packs as many bin runs (or
+// pieces of runs) into a stage as fit, so a stage usually holds several
+// runs and a consumer warp synchronises once per stage, not once per run.
+constexpr int kStageAtoms = 128;
+
 template <int K, bool VEC, bool COUNT>
-__global__ void __launch_bounds__(kBrickThreads) cutoff_brick_kernel(const __grid_constant__ BrickParams p) {
-    constexpr int kStageSlots = kRunMaxBins * K;
-    __shared__ __align__(128) float4 ring[kBrickStages][kStageSlots];
+__global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __grid_constant__ BrickParams p) {
+    __shared__ __align__(128) float4 ring[kBrickStages][kStageAtoms];
+    __shared__ __align__(16) AtomPair wlist[kBrickConsumerWarps][kStageAtoms];
     __shared__ uint64_t full[kBrickStages], empty[kBrickStages];
     __shared__ volatile int stage_n[kBrickStages];
 
@@ -280,89 +292,137 @@ __global__ void __launch_bounds__(kBrickThreads) cutoff_brick_kernel(const __gri
 
     if (warp == kBrickConsumerWarps) {
         // ------------------------------------------------------------ producer
+        // Lane 0 issues every copy; the other lanes load bin counts and
+        // starts for it.  Stage s of use u is refilled only after the four
+        // consumer warps released use u-1 (empty[s]); full[s] completes when
+        // lane 0 has arrived and all bytes of the stage's copies landed.
         const int hx = brick_home_dev(bx, p.m, p.h64, p.b64);
         const int hy = brick_home_dev(by, p.m, p.h64, p.b64);
         const int hz = brick_home_dev(bz, p.m, p.h64, p.b64);
-        int seq = 0;
-        bool ok = true;
-        // lane 0 only: next stage, after its previous contents are consumed
-        auto acquire_stage = [&]() -> int {
-            const int s = seq % kBrickStages;
+        int seq = 0, fill = 0, cur = 0;
+        bool open = false, ok = true;
+        auto open_stage = [&]() {
+            cur = seq % kBrickStages;
             const int use = seq / kBrickStages;
-            if (use > 0 && ok) ok = mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), p.status);
-            return s;
+            if (use > 0 && ok) ok = mbar_wait(&empty[cur], (uint32_t)((use - 1) & 1), p.status);
+            fill = 0;
+            open = true;
         };
-        auto emit = [&](const float4 *src, int nslots) {
-            const int s = acquire_stage();
-            if (ok) {
-                stage_n[s] = nslots;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)nslots * 16u);
-                bulk_g2s(&ring[s][0], src, (uint32_t)nslots * 16u, &full[s]);
-            }
+        auto close_stage = [&]() {
+            stage_n[cur] = fill;
+            mbar_arrive(&full[cur]);
             ++seq;
+            open = false;
         };
-        for (int pass = 0; pass < 2; ++pass) {
-            for (int r = 0; r < p.n_runs && ok; ++r) {
-                const int code = p.runs[r];
-                const int dy = (int)(signed char)(code & 0xff);
-                const int dz = (int)(signed char)((code >> 8) & 0xff);
-                const int dxl = (int)(signed char)((code >> 16) & 0xff);
-                const int dxh = (int)(signed char)((code >> 24) & 0xff);
-                const int uy = hy + dy, uz = hz + dz;
-                if (uy < 0 || uy >= p.nb[1] || uz < 0 || uz >= p.nb[2]) continue;
-                const int xlo = max(hx + dxl, 0), xhi = min(hx + dxh, p.nb[0] - 1);
-                if (xlo > xhi) continue;
-                const int first = (uz * p.nb[1] + uy) * p.nb[0] + xlo;
-                const int nbin = xhi - xlo + 1;
-                const int cnt = lane < nbin ? p.count[first + lane] : 0;
-                if (pass == 0) {
-                    const unsigned nz = __ballot_sync(0xffffffffu, cnt > 0);
-                    if (nz != 0u) {
-                        const int l0 = __ffs(nz) - 1, l1 = 31 - __clz(nz);
-                        if (lane == 0) emit(p.padded + (long long)(first + l0) * K, (l1 - l0 + 1) * K);
-                    }
-                } else {
-                    const int st = lane < nbin ? p.start[first + lane] : 0;
-                    unsigned ov = __ballot_sync(0xffffffffu, cnt > K);
-                    while (ov != 0u) {
-                        const int j = __ffs(ov) - 1;
-                        ov &= ov - 1u;
-                        const int cj = __shfl_sync(0xffffffffu, cnt, j);
-                        const int sj = __shfl_sync(0xffffffffu, st, j);
-                        if (lane == 0) {
-                            for (int off = K; off < cj && ok; off += kStageSlots)
-                                emit(p.csr_atoms + sj + off, min(kStageSlots, cj - off));
-                        }
+        // queue n atoms starting at src (lane 0 only)
+        auto push = [&](const float4 *src, int n) {
+            while (n > 0 && ok) {
+                if (!open) open_stage();
+                const int take = min(n, kStageAtoms - fill);
+                mbar_expect_tx(&full[cur], (uint32_t)take * 16u);
+                bulk_g2s(&ring[cur][fill], src, (uint32_t)take * 16u, &full[cur]);
+                fill += take;
+                src += take;
+                n -= take;
+                if (fill == kStageAtoms) close_stage();
+            }
+        };
+        // bins of run r, clamped to the bin grid: first bin and count (0 if none)
+        auto run_bins = [&](int r, int &first, int &nbin) {
+            const int code = p.runs[r];
+            const int dy = (int)(signed char)(code & 0xff);
+            const int dz = (int)(signed char)((code >> 8) & 0xff);
+            const int dxl = (int)(signed char)((code >> 16) & 0xff);
+            const int dxh = (int)(signed char)((code >> 24) & 0xff);
+            const int uy = hy + dy, uz = hz + dz;
+            const int xlo = max(hx + dxl, 0), xhi = min(hx + dxh, p.nb[0] - 1);
+            first = (uz * p.nb[1] + uy) * p.nb[0] + xlo;
+            nbin = (uy < 0 || uy >= p.nb[1] || uz < 0 || uz >= p.nb[2] || xlo > xhi) ? 0 : xhi - xlo + 1;
+        };
+        if (K == 0) {
+            // bin-sorted atoms of a run of consecutive bins are contiguous:
+            // one copy of [start[first], start[first + nbin]) per run
+            for (int r0 = 0; r0 < p.n_runs && ok; r0 += 32) {
+                int lo = 0, hi = 0;
+                if (r0 + lane < p.n_runs) {
+                    int first, nbin;
+                    run_bins(r0 + lane, first, nbin);
+                    if (nbin > 0) {
+                        lo = p.start[first];
+                        hi = p.start[first + nbin];
                     }
                 }
+                const int nr = min(32, p.n_runs - r0);
+                for (int t = 0; t < nr; ++t) {
+                    const int l = __shfl_sync(0xffffffffu, lo, t);
+                    const int h = __shfl_sync(0xffffffffu, hi, t);
+                    if (lane == 0 && h > l) push(p.csr_atoms + l, h - l);
+                }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                seq = __shfl_sync(0xffffffffu, seq, 0);
+            }
+        } else {
+            // fixed-capacity slots of each run (trimmed to its occupied
+            // bins), then the overflow of the bins holding more than K
+            for (int pass = 0; pass < 2; ++pass) {
+                for (int r = 0; r < p.n_runs && ok; ++r) {
+                    int first, nbin;
+                    run_bins(r, first, nbin);
+                    for (int cb = 0; cb < nbin && ok; cb += 32) {  // 32 bins per step
+                        const int nb32 = min(32, nbin - cb);
+                        const int f32 = first + cb;
+                        const int cnt = lane < nb32 ? p.count[f32 + lane] : 0;
+                        if (pass == 0) {
+                            const unsigned nz = __ballot_sync(0xffffffffu, cnt > 0);
+                            if (nz != 0u && lane == 0) {
+                                const int l0 = __ffs(nz) - 1, l1 = 31 - __clz(nz);
+                                push(p.padded + (long long)(f32 + l0) * K, (l1 - l0 + 1) * K);
+                            }
+                        } else {
+                            const int st = lane < nb32 ? p.start[f32 + lane] : 0;
+                            unsigned ov = __ballot_sync(0xffffffffu, cnt > K);
+                            while (ov != 0u) {
+                                const int jb = __ffs(ov) - 1;
+                                ov &= ov - 1u;
+                                const int cj = __shfl_sync(0xffffffffu, cnt, jb);
+                                const int sj = __shfl_sync(0xffffffffu, st, jb);
+                                if (lane == 0) push(p.csr_atoms + sj + K, cj - K);
+                            }
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                    }
+                }
             }
         }
-        if (lane == 0) {  // end of stream
-            const int s = acquire_stage();
-            stage_n[s] = -1;
-            mbar_arrive(&full[s]);
+        if (lane == 0) {
+            if (open) close_stage();
+            open_stage();  // end of stream
+            stage_n[cur] = -1;
+            mbar_arrive(&full[cur]);
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    // this lane's points: x = 8bx + xq .. +3, y = 8by + yy, z = 8bz + zz
+    // A lane owns 4 consecutive x points (two f32x2 pairs) of one y row and z
+    // plane: x = 8bx + xq .. +3, y = 8by + yy, z = 8bz + zz.  Warp w covers
+    // an 8 x 4 x 4-point sub-box of the brick.
     const int xq = (lane & 1) * 4;
     const int yy = (warp & 1) * 4 + ((lane >> 1) & 3);
     const int zz = (warp >> 1) * 4 + (lane >> 3);
     const int i0 = kBrick * bx + xq, j = kBrick * by + yy, k = kBrick * bz + zz;
-    float x[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) x[c] = fmaf((float)(i0 + c), p.h, p.ox);
+    const float2 X01 = make_float2(fmaf((float)(i0 + 0), p.h, p.ox), fmaf((float)(i0 + 1), p.h, p.ox));
+    const float2 X23 = make_float2(fmaf((float)(i0 + 2), p.h, p.ox), fmaf((float)(i0 + 3), p.h, p.ox));
     const float y = fmaf((float)j, p.h, p.oy);
     const float z = fmaf((float)k, p.h, p.oz);
-    // the warp's sub-box (8 x 4 x 4 points), from the same coordinate formula
+    const float2 Y2 = make_float2(y, y), Z2 = make_float2(z, z);
+    const float2 NG0 = make_float2(-p.gc0, -p.gc0), NG1 = make_float2(-p.gc1, -p.gc1);
+    const float2 NG2 = make_float2(-p.gc2, -p.gc2);
+    // the warp's sub-box, from the same coordinate formula as the points
     const float lox = fmaf((float)(kBrick * bx), p.h, p.ox), hix = fmaf((float)(kBrick * bx + 7), p.h, p.ox);
     const int jb = kBrick * by + (warp & 1) * 4, kb = kBrick * bz + (warp >> 1) * 4;
     const float loy = fmaf((float)jb, p.h, p.oy), hiy = fmaf((float)(jb + 3), p.h, p.oy);
     const float loz = fmaf((float)kb, p.h, p.oz), hiz = fmaf((float)(kb + 3), p.h, p.oz);
+    AtomPair *list = wlist[warp];
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     unsigned long long n_real = 0, n_near = 0, n_useful = 0;  // COUNT only
@@ -371,47 +431,69 @@ __global__ void __launch_bounds__(kBrickThreads) cutoff_brick_kernel(const __gri
         if (!mbar_wait(&full[s], (uint32_t)((seq / kBrickStages) & 1), p.status)) break;
         const int n = stage_n[s];
         if (n < 0) break;
+        // (1) keep the atoms that can reach a point of this warp's sub-box:
+        // 32 slots per step, compacted into the warp's list (each component
+        // stored twice, coordinates negated, for the f32x2 pair loop)
         const float4 *slots = &ring[s][0];
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        int cnt = 0;  // atoms listed for this warp
         for (int base = 0; base < n; base += 32) {
             bool near = false;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
             if (base + lane < n) {
-                const float4 a = slots[base + lane];
+                a = slots[base + lane];
                 const float ex = fmaxf(fmaxf(lox - a.x, a.x - hix), 0.0f);
                 const float ey = fmaxf(fmaxf(loy - a.y, a.y - hiy), 0.0f);
                 const float ez = fmaxf(fmaxf(loz - a.z, a.z - hiz), 0.0f);
                 near = fmaf(ex, ex, fmaf(ey, ey, ez * ez)) < p.cull2;
                 if (COUNT && a.x < 1.0e17f) ++n_real;
             }
-            unsigned mask = __ballot_sync(0xffffffffu, near);
-            if (COUNT && lane == 0) n_near += __popc(mask);
-            while (mask != 0u) {
-                const int t = __ffs(mask) - 1;
-                mask &= mask - 1u;
-                const float4 a = slots[base + t];  // broadcast
-                const float dy = y - a.y, dz = z - a.z;
-                const float dyz2 = fmaf(dy, dy, dz * dz);
+            const unsigned mask = __ballot_sync(0xffffffffu, near);
+            if (near) {
+                const int pos = cnt + __popc(mask & ((1u << lane) - 1u));
+                list[pos] = AtomPair{make_float2(-a.x, -a.x), make_float2(-a.y, -a.y), make_float2(-a.z, -a.z),
+                                     make_float2(a.w, a.w)};
+            }
+            cnt += __popc(mask);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // the stage is free again
+        if (COUNT) n_near += (unsigned)cnt;
+        // (2) every listed atom against the lane's 4 points
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+        for (int t = 0; t < cnt; ++t) {
+            const AtomPair a = list[t];  // broadcast
+            const float2 dy = __fadd2_rn(Y2, a.y);
+            const float2 dz = __fadd2_rn(Z2, a.z);
+            const float2 dyz2 = __ffma2_rn(dy, dy, __fmul2_rn(dz, dz));
+            const float2 dx01 = __fadd2_rn(X01, a.x);
+            const float2 dx23 = __fadd2_rn(X23, a.x);
+            const float2 r01 = __ffma2_rn(dx01, dx01, dyz2);
+            const float2 r23 = __ffma2_rn(dx23, dx23, dyz2);
+            // e = rsqrt(r^2) - g(r^2), with -g by Horner on the negated coefficients
+            const float2 rs01 = make_float2(sfu_rsqrt(r01.x), sfu_rsqrt(r01.y));
+            const float2 rs23 = make_float2(sfu_rsqrt(r23.x), sfu_rsqrt(r23.y));
+            const float2 e01 = __fadd2_rn(rs01, __ffma2_rn(__ffma2_rn(r01, NG2, NG1), r01, NG0));
+            const float2 e23 = __fadd2_rn(rs23, __ffma2_rn(__ffma2_rn(r23, NG2, NG1), r23, NG0));
+            if (r01.x < p.c2) part[0] = fmaf(a.q.x, e01.x, part[0]);
+            if (r01.y < p.c2) part[1] = fmaf(a.q.x, e01.y, part[1]);
+            if (r23.x < p.c2) part[2] = fmaf(a.q.x, e23.x, part[2]);
+            if (r23.y < p.c2) part[3] = fmaf(a.q.x, e23.y, part[3]);
+            if (COUNT) {
+                const float r2c[4] = {r01.x, r01.y, r23.x, r23.y};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float dx = x[c] - a.x;
-                    const float r2 = fmaf(dx, dx, dyz2);
-                    const float g = fmaf(fmaf(r2, p.gc2, p.gc1), r2, p.gc0);
-                    const float e = sfu_rsqrt(r2) - g;
-                    if (r2 < p.c2) part[c] = fmaf(a.w, e, part[c]);
-                    if (COUNT && r2 < p.c2 && i0 + c < p.nx && j < p.ny && k < p.nz) ++n_useful;
-                }
+                for (int c = 0; c < 4; ++c)
+                    if (r2c[c] < p.c2 && i0 + c < p.nx && j < p.ny && k < p.nz) ++n_useful;
             }
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[c] += part[c];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        __syncwarp();  // the list is rewritten by the next stage
     }
 
     if (COUNT) {
-        // per warp: real atoms seen and atoms past the sub-box test, each
-        // examined against the warp's 128 points; useful = pairs with r < c
-        // at stored points
+        // per warp: real atoms seen and atoms listed, each examined against
+        // the warp's 128 points; useful = pairs with r < c at stored points
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             n_real += __shfl_down_sync(0xffffffffu, n_real, o);
@@ -562,6 +644,15 @@ int launch_bricks_k(const Prepared &P, const OffsetList &L, float *V, cudaStream
     return CP_OK;
 }
 
+int launch_bricks(const Prepared &P, const OffsetList &L, float *V, cudaStream_t stream,
+                  unsigned long long *counts = nullptr) {
+    switch (P.bp.K) {
+        case 0: return launch_bricks_k<0>(P, L, V, stream, counts);
+        case 8: return launch_bricks_k<8>(P, L, V, stream, counts);
+        default: return launch_bricks_k<16>(P, L, V, stream, counts);
+    }
+}
+
 }  // namespace
 
 }  // namespace cpmap
@@ -594,7 +685,7 @@ CP_API int cp_cutoff(const float *atoms, int n_atoms, int nx, int ny, int nz, cp
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = launch_binning(P, s);
     if (rc) return rc;
-    return capacity == 8 ? launch_bricks_k<8>(P, L, V, s) : launch_bricks_k<16>(P, L, V, s);
+    return launch_bricks(P, L, V, s);
 }
 
 CP_API int cp_cutoff_map(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
@@ -610,7 +701,7 @@ CP_API int cp_cutoff_map(const float *atoms, int n_atoms, int nx, int ny, int nz
     rc = make_offset_list(P.g, P.bg, &L);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return capacity == 8 ? launch_bricks_k<8>(P, L, V, s) : launch_bricks_k<16>(P, L, V, s);
+    return launch_bricks(P, L, V, s);
 }
 
 CP_API int cp_cutoff_pair_counts(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
@@ -629,8 +720,7 @@ CP_API int cp_cutoff_pair_counts(const float *atoms, int n_atoms, int nx, int ny
     if (cudaMemsetAsync(counts, 0, 3 * sizeof(unsigned long long), s) != cudaSuccess) return CP_ERR_CUDA;
     rc = launch_binning(P, s);
     if (rc) return rc;
-    return capacity == 8 ? launch_bricks_k<8>(P, L, nullptr, s, counts)
-                         : launch_bricks_k<16>(P, L, nullptr, s, counts);
+    return launch_bricks(P, L, nullptr, s, counts);
 }
 
 CP_API int cp_cutoff_stats(const void *workspace, size_t workspace_bytes, int n_atoms, int nx, int ny, int nz,
@@ -722,7 +812,7 @@ CP_API int cp_cutoff_no_alloc(const float *atoms, int n_atoms, int nx, int ny, i
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = launch_binning(P, s);
     if (rc) return rc;
-    return capacity == 8 ? launch_bricks_k<8>(P, OL, V, s) : launch_bricks_k<16>(P, OL, V, s);
+    return launch_bricks(P, OL, V, s);
 }
 
 }  // extern "C"

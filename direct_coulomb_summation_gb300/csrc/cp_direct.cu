@@ -41,9 +41,12 @@ namespace cg = cooperative_groups;
 namespace cpmap {
 
 constexpr int kDirectThreads = 128;
-constexpr int kDirectTile = 512;  // atoms per shared-memory stage (8 KiB)
+constexpr int kDirectTile = 256;  // atoms per shared-memory stage (4 KiB as loaded)
 constexpr int kDirectStages = 3;
-constexpr int kDirectSmem = kDirectStages * kDirectTile * 16;
+// dynamic shared memory: the TMA ring of raw atoms, then the expanded tile
+// (each atom as (-x,-x), (-y,-y), (-z,-z), (q,q): 32 bytes)
+constexpr int kDirectRingBytes = kDirectStages * kDirectTile * 16;
+constexpr int kDirectSmem = kDirectRingBytes + kDirectTile * 32;
 constexpr int kMaxSplit = 8;  // portable cluster size
 
 struct DirectParams {
@@ -57,6 +60,12 @@ struct DirectParams {
     long long npatch;
     float *V;
     unsigned int *status;
+};
+
+// One expanded atom: coordinates negated and every component duplicated, so
+// that point - atom and q * rsqrt are single f32x2 operations.
+struct __align__(16) DupAtom {
+    float2 x, y, z, q;
 };
 
 // Stores one x quad of row (y, z): a float4 when the row is 16-byte aligned
@@ -75,11 +84,17 @@ __device__ __forceinline__ void store_quad(const DirectParams &p, int i0, int y,
     }
 }
 
-template <int PY, int PZ, bool VEC>
+// A thread owns 4 x points (two f32x2 pairs) x PY rows x PZ planes, i.e.
+// 2*PY*PZ point pairs.  The first EMU pairs take their rsqrt on the FMA pipe
+// (fma_rsqrt2), the others on the SFU, so that both units share the work.
+template <int PY, int PZ, int EMU, bool VEC>
 __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_constant__ DirectParams p) {
+    constexpr int NP = 2 * PY * PZ;  // point pairs per thread
+    static_assert(EMU >= 0 && EMU <= NP, "EMU counts point pairs");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[kDirectStages];
     float4 *ring = reinterpret_cast<float4 *>(smem);
+    DupAtom *tile = reinterpret_cast<DupAtom *>(smem + kDirectRingBytes);
 
     const int tid = threadIdx.x;
     const int split = p.split;
@@ -101,13 +116,19 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
     const int yb = (int)(t % p.yb);
     const int zb = (int)(t / p.yb);
     const int i0 = 4 * qx, j0 = PY * yb, k0 = PZ * zb;
-    float x[4], y[PY], z[PZ];
+    const float2 X01 = make_float2(fmaf((float)(i0 + 0), p.h, p.ox), fmaf((float)(i0 + 1), p.h, p.ox));
+    const float2 X23 = make_float2(fmaf((float)(i0 + 2), p.h, p.ox), fmaf((float)(i0 + 3), p.h, p.ox));
+    float2 Y[PY], Z[PZ];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) x[c] = fmaf((float)(i0 + c), p.h, p.ox);
+    for (int j = 0; j < PY; ++j) {
+        const float y = fmaf((float)(j0 + j), p.h, p.oy);
+        Y[j] = make_float2(y, y);
+    }
 #pragma unroll
-    for (int j = 0; j < PY; ++j) y[j] = fmaf((float)(j0 + j), p.h, p.oy);
-#pragma unroll
-    for (int k = 0; k < PZ; ++k) z[k] = fmaf((float)(k0 + k), p.h, p.oz);
+    for (int k = 0; k < PZ; ++k) {
+        const float z = fmaf((float)(k0 + k), p.h, p.oz);
+        Z[k] = make_float2(z, z);
+    }
 
     if (tid == 0) {
         for (int s = 0; s < kDirectStages; ++s) mbar_init(&full[s], 1);
@@ -115,72 +136,74 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
     }
     __syncthreads();
 
-    auto issue = [&](int tile, int stage) {
-        const int n = min(kDirectTile, n_local - tile * kDirectTile);
+    auto issue = [&](int tl, int stage) {
+        const int n = min(kDirectTile, n_local - tl * kDirectTile);
         const uint32_t bytes = (uint32_t)n * 16u;
         mbar_arrive_expect_tx(&full[stage], bytes);
-        bulk_g2s(ring + stage * kDirectTile, p.atoms + a_begin + (long long)tile * kDirectTile, bytes, &full[stage]);
+        bulk_g2s(ring + stage * kDirectTile, p.atoms + a_begin + (long long)tl * kDirectTile, bytes, &full[stage]);
     };
     if (tid == 0) {
         for (int s = 0; s < kDirectStages && s < n_tiles; ++s) issue(s, s);
     }
 
-    float acc[PZ][PY][4];
+    // acc[(k*PY + j)*2 + h]: pair h (points 0,1 or 2,3) of row j, plane k
+    float2 acc[NP];
 #pragma unroll
-    for (int k = 0; k < PZ; ++k)
-#pragma unroll
-        for (int j = 0; j < PY; ++j)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[k][j][c] = 0.0f;
+    for (int q = 0; q < NP; ++q) acc[q] = make_float2(0.f, 0.f);
 
     for (int it = 0; it < n_tiles; ++it) {
         const int stage = it % kDirectStages;
         mbar_wait(&full[stage], (uint32_t)((it / kDirectStages) & 1), p.status);
-        const float4 *tile = ring + stage * kDirectTile;
         const int n = min(kDirectTile, n_local - it * kDirectTile);
+        const float4 *raw = ring + stage * kDirectTile;
+        for (int a = tid; a < n; a += kDirectThreads) {
+            const float4 v = raw[a];
+            tile[a] = DupAtom{make_float2(-v.x, -v.x), make_float2(-v.y, -v.y), make_float2(-v.z, -v.z),
+                              make_float2(v.w, v.w)};
+        }
+        __syncthreads();  // the expanded tile is ready, the raw stage is free
+        if (tid == 0 && it + kDirectStages < n_tiles) issue(it + kDirectStages, stage);
 
-        float part[PZ][PY][4];
+        float2 part[NP];
 #pragma unroll
-        for (int k = 0; k < PZ; ++k)
-#pragma unroll
-            for (int j = 0; j < PY; ++j)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) part[k][j][c] = 0.0f;
+        for (int q = 0; q < NP; ++q) part[q] = make_float2(0.f, 0.f);
 
 #pragma unroll 2
         for (int a = 0; a < n; ++a) {
-            const float4 at = tile[a];  // same address in every lane: broadcast
-            float dx[4], dy2[PY];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) dx[c] = x[c] - at.x;
+            const DupAtom at = tile[a];  // same address in every lane: broadcast
+            const float2 dx01 = __fadd2_rn(X01, at.x);
+            const float2 dx23 = __fadd2_rn(X23, at.x);
+            float2 dy2[PY];
 #pragma unroll
             for (int j = 0; j < PY; ++j) {
-                const float dy = y[j] - at.y;
-                dy2[j] = dy * dy;
+                const float2 dy = __fadd2_rn(Y[j], at.y);
+                dy2[j] = __fmul2_rn(dy, dy);
             }
 #pragma unroll
             for (int k = 0; k < PZ; ++k) {
-                const float dz = z[k] - at.z;
+                const float2 dz = __fadd2_rn(Z[k], at.z);
 #pragma unroll
                 for (int j = 0; j < PY; ++j) {
-                    const float dyz2 = fmaf(dz, dz, dy2[j]);
+                    const float2 dyz2 = __ffma2_rn(dz, dz, dy2[j]);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float r2 = fmaf(dx[c], dx[c], dyz2);
-                        part[k][j][c] = fmaf(at.w, sfu_rsqrt(r2), part[k][j][c]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int q = (k * PY + j) * 2 + hh;
+                        const float2 dx = hh == 0 ? dx01 : dx23;
+                        const float2 r2 = __ffma2_rn(dx, dx, dyz2);
+                        float2 rs;
+                        if (q < EMU) {
+                            rs = fma_rsqrt2(r2);
+                        } else {
+                            rs = make_float2(sfu_rsqrt(r2.x), sfu_rsqrt(r2.y));
+                        }
+                        part[q] = __ffma2_rn(at.q, rs, part[q]);
                     }
                 }
             }
         }
 #pragma unroll
-        for (int k = 0; k < PZ; ++k)
-#pragma unroll
-            for (int j = 0; j < PY; ++j)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[k][j][c] += part[k][j][c];
-
-        __syncthreads();  // every thread is done with this stage
-        if (tid == 0 && it + kDirectStages < n_tiles) issue(it + kDirectStages, stage);
+        for (int q = 0; q < NP; ++q) acc[q] = __fadd2_rn(acc[q], part[q]);
+        __syncthreads();  // every thread is done with the expanded tile
     }
 
     if (split == 1) {
@@ -188,9 +211,10 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
 #pragma unroll
             for (int k = 0; k < PZ; ++k)
 #pragma unroll
-                for (int j = 0; j < PY; ++j)
-                    store_quad<VEC>(p, i0, j0 + j, k0 + k,
-                                    make_float4(acc[k][j][0], acc[k][j][1], acc[k][j][2], acc[k][j][3]));
+                for (int j = 0; j < PY; ++j) {
+                    const float2 a01 = acc[(k * PY + j) * 2], a23 = acc[(k * PY + j) * 2 + 1];
+                    store_quad<VEC>(p, i0, j0 + j, k0 + k, make_float4(a01.x, a01.y, a23.x, a23.y));
+                }
         }
         return;
     }
@@ -203,9 +227,10 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
 #pragma unroll
     for (int k = 0; k < PZ; ++k)
 #pragma unroll
-        for (int j = 0; j < PY; ++j)
-            partial[(k * PY + j) * kDirectThreads + tid] =
-                make_float4(acc[k][j][0], acc[k][j][1], acc[k][j][2], acc[k][j][3]);
+        for (int j = 0; j < PY; ++j) {
+            const float2 a01 = acc[(k * PY + j) * 2], a23 = acc[(k * PY + j) * 2 + 1];
+            partial[(k * PY + j) * kDirectThreads + tid] = make_float4(a01.x, a01.y, a23.x, a23.y);
+        }
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     const int n_elem = R * kDirectThreads;
@@ -241,17 +266,16 @@ namespace {
 using KernelFn = void (*)(DirectParams);
 
 struct Variant {
-    int py, pz;
+    int py, pz, emu;
     KernelFn vec, scalar;
 };
 
+#define CP_VARIANT(PY, PZ, EMU) {PY, PZ, EMU, direct_kernel<PY, PZ, EMU, true>, direct_kernel<PY, PZ, EMU, false>}
 const Variant kVariants[] = {
-    {4, 2, direct_kernel<4, 2, true>, direct_kernel<4, 2, false>},
-    {2, 2, direct_kernel<2, 2, true>, direct_kernel<2, 2, false>},
-    {4, 1, direct_kernel<4, 1, true>, direct_kernel<4, 1, false>},
-    {2, 1, direct_kernel<2, 1, true>, direct_kernel<2, 1, false>},
-    {1, 1, direct_kernel<1, 1, true>, direct_kernel<1, 1, false>},
+    CP_VARIANT(4, 2, 0), CP_VARIANT(2, 2, 0), CP_VARIANT(4, 1, 0), CP_VARIANT(2, 1, 0), CP_VARIANT(1, 1, 0),
+    CP_VARIANT(4, 2, 4), CP_VARIANT(4, 2, 5), CP_VARIANT(2, 2, 2), CP_VARIANT(4, 1, 2), CP_VARIANT(2, 1, 1),
 };
+#undef CP_VARIANT
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
 // Resident CTAs per GPU for variant v and cluster size s (cached per device).
@@ -297,8 +321,23 @@ struct Plan {
     long long npatch;
 };
 
+// Modelled pairs per SM clock of a patch shape: the slowest of the SFU
+// (16 rsqrt/clk), the FMA pipe (about 125 fp32 lane operations/clk; an
+// f32x2 instruction counts two) and instruction issue (4 warp instructions,
+// i.e. 128 thread instructions, per clk), per atom and thread.
+double variant_rate(int py, int pz, int emu) {
+    const double P = 4.0 * py * pz;        // points per thread
+    const double npair = P / 2.0;          // f32x2 point pairs
+    const double sfu = P - 2.0 * emu;      // rsqrt on the SFU
+    const double issue = 2.0 + 2.0 + 2.0 * py + pz + py * pz + 2.0 * npair + sfu + 11.0 * emu + 1.0;
+    const double fma = 4.0 + 4.0 * py + 2.0 * pz + 2.0 * py * pz + 2.0 * P + 14.0 * emu;
+    const double clk = std::max(sfu / 16.0, std::max(fma / 125.0, issue / 128.0));
+    return P / clk;
+}
+
 // Picks the patch shape and cluster split with the smallest modelled time:
-// waves x (points per CTA) x (atoms per CTA), plus a fixed cost per CTA wave.
+// CTA waves x the time one CTA takes while sharing its SM with the other
+// resident CTAs, plus a fixed cost per CTA.
 int plan_direct(const Grid &g, int n_atoms, bool vec, const DeviceInfo &dev, Plan *out) {
     double best = INFINITY;
     for (int v = 0; v < kNumVariants; ++v) {
@@ -309,17 +348,16 @@ int plan_direct(const Grid &g, int n_atoms, bool vec, const DeviceInfo &dev, Pla
         const long long npatch = qx * yb * zb;
         const long long ctas = (npatch + kDirectThreads - 1) / kDirectThreads;
         const double pts = (double)kDirectThreads * 4 * py * pz;
+        const double rate = variant_rate(py, pz, kVariants[v].emu);
         for (int s = 1; s <= kMaxSplit; ++s) {
             if (s > 1 && (long long)n_atoms < (long long)s * 64) break;
             if (ctas * s > 0x7fffffffll) break;
             const int slots = resident_ctas(v, s, vec, dev);
             if (slots < 0) return CP_ERR_CUDA;
             const double waves = std::ceil((double)(ctas * s) / slots);
+            const double per_sm = (double)slots / dev.sm_count;
             const double atoms = std::max(1.0, (double)n_atoms / s);
-            // small patches pay more issue slots per pair (x differences and
-            // row sums are amortised over fewer points)
-            const double issue = 3.0 + (5.0 + 2.0 * py + pz + py * pz) / (4.0 * py * pz);
-            const double t = waves * (pts * atoms * std::max(1.0, issue / 7.0) + 4.0e4);
+            const double t = waves * (pts * atoms * per_sm / rate + 3000.0);
             if (t < best * 0.98) {
                 best = t;
                 out->variant = v;

@@ -39,7 +39,7 @@ int check_grid(int nx, int ny, int nz, cp_vec3 origin, float h, Grid *g) {
 int check_cutoff_args(const Grid &, float cutoff, float bin_size, int capacity) {
     if (!std::isfinite(cutoff) || !(cutoff > 0.0f)) return CP_ERR_INVALID_ARGUMENT;
     if (!std::isfinite(bin_size) || !(bin_size > 0.0f)) return CP_ERR_INVALID_ARGUMENT;
-    if (capacity != 8 && capacity != 16) return CP_ERR_UNSUPPORTED;
+    if (capacity != 0 && capacity != 8 && capacity != 16) return CP_ERR_UNSUPPORTED;
     return CP_OK;
 }
 
@@ -139,31 +139,24 @@ int make_offset_list(const Grid &g, const BinGeom &bg, OffsetList *out) {
             const double gy = ax[1].gap[dy - ax[1].lo];
             const double gyz = gy * gy + gz * gz;
             if (!(gyz < r2)) continue;
-            int run_lo = 0, run_len = 0;
-            auto flush = [&]() -> bool {
-                if (run_len == 0) return true;
-                if (nr >= kMaxRuns) return false;
-                out->run[nr][0] = (int8_t)dy;
-                out->run[nr][1] = (int8_t)dz;
-                out->run[nr][2] = (int8_t)run_lo;
-                out->run[nr][3] = (int8_t)(run_lo + run_len - 1);
-                ++nr;
-                nbins += run_len;
-                run_len = 0;
-                return true;
-            };
+            // the listed dx of one (dy, dz) row form an interval (the per-axis
+            // minimum gap falls and then rises with dx); one run covers it
+            int run_lo = 0, run_hi = -1;
             for (int dx = ax[0].lo; dx <= ax[0].hi; ++dx) {
                 const double gx = ax[0].gap[dx - ax[0].lo];
-                const bool in = (gx * gx + gyz) < r2;
-                if (in) {
-                    if (run_len == 0) run_lo = dx;
-                    ++run_len;
-                    if (run_len == kRunMaxBins && !flush()) return CP_ERR_TOO_LARGE;
-                } else if (!flush()) {
-                    return CP_ERR_TOO_LARGE;
+                if ((gx * gx + gyz) < r2) {
+                    if (run_hi < run_lo) run_lo = dx;
+                    run_hi = dx;
                 }
             }
-            if (!flush()) return CP_ERR_TOO_LARGE;
+            if (run_hi < run_lo) continue;
+            if (nr >= kMaxRuns) return CP_ERR_TOO_LARGE;
+            out->run[nr][0] = (int8_t)dy;
+            out->run[nr][1] = (int8_t)dz;
+            out->run[nr][2] = (int8_t)run_lo;
+            out->run[nr][3] = (int8_t)run_hi;
+            ++nr;
+            nbins += run_hi - run_lo + 1;
         }
     }
     out->n_runs = nr;

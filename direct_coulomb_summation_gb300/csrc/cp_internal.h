@@ -14,7 +14,6 @@ namespace cpmap {
 
 constexpr int kBrick = 8;            // brick edge in grid points (8x8x8 = 512 points)
 constexpr int kMaxRuns = 1024;       // offset-list x-runs a brick kernel can take
-constexpr int kRunMaxBins = 8;       // bins per x-run (longer runs are split)
 constexpr float kPadCoord = 1.0e18f; // position of an unused bin slot
 constexpr int kScanBlock = 2048;     // bins per block of the count scan
 constexpr int kMaxScanBlocks = 8192; // so at most 16M bins

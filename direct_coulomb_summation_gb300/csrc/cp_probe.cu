@@ -59,11 +59,40 @@ __global__ void probe_kernel(int iters, float seed, long long *cycles, float *si
     if (s == 12345.678f) sink[threadIdx.x] = s;  // keeps the chains alive
 }
 
+template <int KIND>
+__global__ void eval_rsqrt_kernel(const float *x, float *y, int n) {
+    const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (i >= n) return;
+    const float2 v = make_float2(x[i], i + 1 < n ? x[i + 1] : 1.0f);
+    float2 r;
+    if (KIND == 0)
+        r = make_float2(sfu_rsqrt(v.x), sfu_rsqrt(v.y));
+    else
+        r = fma_rsqrt2(v);
+    y[i] = r.x;
+    if (i + 1 < n) y[i + 1] = r.y;
+}
+
 }  // namespace cpmap
 
 using namespace cpmap;
 
 extern "C" {
+
+CP_API int cp_eval_rsqrt(int kind, const float *x, float *y, int n, void *stream) {
+    if ((kind != 0 && kind != 1) || n < 0 || (n > 0 && (!x || !y))) return CP_ERR_INVALID_ARGUMENT;
+    if (n == 0) return CP_OK;
+    const int threads = 256;
+    const int blocks = (int)(((long long)(n + 1) / 2 + threads - 1) / threads);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (kind == 0)
+        eval_rsqrt_kernel<0><<<blocks, threads, 0, s>>>(x, y, n);
+    else
+        eval_rsqrt_kernel<1><<<blocks, threads, 0, s>>>(x, y, n);
+    if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
+    note_launches(1);
+    return CP_OK;
+}
 
 CP_API int cp_probe_pipe_rate(int kind, int warps, int iters, double *ops_per_clk, double *ms, void *stream) {
     if (kind < 0 || kind > 3 || warps < 1 || warps > 32 || iters < 1 || !ops_per_clk) return CP_ERR_INVALID_ARGUMENT;

@@ -72,7 +72,7 @@ typedef enum {
     CP_ERR_MISALIGNED = -2,        /* atoms or workspace not aligned as required */
     CP_ERR_TOO_LARGE = -3,         /* grid, bin grid or offset list beyond the library's limits */
     CP_ERR_WORKSPACE_TOO_SMALL = -4,
-    CP_ERR_UNSUPPORTED = -5,       /* e.g. a bin capacity other than 8 or 16 */
+    CP_ERR_UNSUPPORTED = -5,       /* e.g. a bin capacity other than 0, 8 or 16 */
     CP_ERR_CUDA = -6,              /* a CUDA runtime call or launch failed */
     CP_ERR_DEVICE = -7             /* a kernel reported a problem (see cp_device_status) */
 } cp_status;
@@ -98,9 +98,12 @@ CP_API int cp_direct(const float *atoms, int n_atoms, int nx, int ny, int nz, cp
                      void *stream);
 
 /* cp_direct with the per-thread point patch and the cluster split forced,
- * for tests and tuning sweeps.  variant: -1 = planner's choice, else the
- * patch of 4 x-points times (PY, PZ) rows/planes with
- * 0 = (4,2), 1 = (2,2), 2 = (4,1), 3 = (2,1), 4 = (1,1).  split: 0 =
+ * for tests and tuning sweeps.  variant: -1 = planner's choice, else a
+ * patch of 4 x-points times PY rows times PZ planes, of whose 2*PY*PZ point
+ * pairs the first EMU take their rsqrt on the FMA pipe instead of the SFU
+ * ((PY, PZ, EMU)): 0 = (4,2,0), 1 = (2,2,0), 2 = (4,1,0), 3 = (2,1,0),
+ * 4 = (1,1,0), 5 = (4,2,4), 6 = (4,2,5), 7 = (2,2,2), 8 = (4,1,2),
+ * 9 = (2,1,1).  split: 0 =
  * planner's choice, else 1..8 CTAs of a cluster share one tile of points and
  * take 1/split of the atoms each (their partial sums meet in distributed
  * shared memory).  Results agree with cp_direct up to fp32 rounding order.
@@ -129,8 +132,13 @@ CP_API int cp_direct_config(const float *atoms, int n_atoms, int nx, int ny, int
  * ("extra atoms", slide "Handling Overfull Bins" (34)); they stay in the
  * bin-sorted array and are swept on the GPU, not on the CPU.
  *
- * A pair contributes iff r^2 < c^2 (strict).  capacity must be 8 (the
- * lecture's 128-byte bins) or 16 (256-byte bins).                          */
+ * A pair contributes iff r^2 < c^2 (strict).  capacity is 8 (the
+ * lecture's 128-byte bins), 16 (256-byte bins) or 0.  With 0 there are no
+ * fixed-capacity slots: the map streams each run of consecutive bins as one
+ * contiguous range of the bin-sorted array (the fixed 128-byte bins were the
+ * lecture's answer to a 64-byte coalescing rule; a TMA bulk copy moves any
+ * 16-byte-aligned range), and every binned atom counts as "overflow" in the
+ * stats.                                                                    */
 
 /* Where each array lives inside a cutoff workspace (byte offsets from its
  * base, each a multiple of 256), for inspection and tests. */
@@ -252,7 +260,8 @@ CP_API int cp_cutoff_stats(const void *workspace, size_t workspace_bytes, int n_
  * (home_x + dx_lo .. home_x + dx_hi, home_y + dy, home_z + dz) of a brick
  * whose home bin is `home`; a bin is listed iff its box can come within
  * c (+ a rounding margin) of some point of some brick (per-axis minimum gap
- * over all bricks, so one list serves every brick).  runs_out receives
+ * over all bricks, so one list serves every brick); there is one run per
+ * (dy, dz).  runs_out receives
  * 4 ints per run (dy, dz, dx_lo, dx_hi); pass NULL to query the sizes.
  * *n_runs and *n_bins receive the list's size.  Returns CP_OK,
  * CP_ERR_INVALID_ARGUMENT, CP_ERR_TOO_LARGE (list longer than the library
@@ -281,6 +290,14 @@ CP_API const char *cp_status_string(int status);
 
 /* Library ABI version (major*10000 + minor*100 + patch). */
 CP_API int cp_version(void);
+
+/* Evaluates n reciprocal square roots of the DEVICE array x into the DEVICE
+ * array y with one of the kernels' two routes: kind 0 = the SFU
+ * (rsqrt.approx.ftz.f32), kind 1 = the FMA-pipe route (magic-constant
+ * estimate and two Newton steps, relative error below 5e-6 for positive
+ * normal x).  For tests of those error bounds.  Returns CP_OK,
+ * CP_ERR_INVALID_ARGUMENT or CP_ERR_CUDA.                                    */
+CP_API int cp_eval_rsqrt(int kind, const float *x, float *y, int n, void *stream);
 
 /* Microbenchmark of one SM pipe: every SM runs `warps` warps, each thread
  * issuing `iters` x 8 independent dependent-chain operations of kind

@@ -75,7 +75,7 @@ def test_direct_rejects_on_host(args, code):
 
 def test_direct_config_rejects_bad_variant():
     lib = cp.library()
-    assert lib.cp_direct_config(FAKE, 5, *GRID, FAKE, 7, 0, None) == -1
+    assert lib.cp_direct_config(FAKE, 5, *GRID, FAKE, 10, 0, None) == -1
     assert lib.cp_direct_config(FAKE, 5, *GRID, FAKE, 0, 9, None) == -1
     assert lib.cp_direct_config(FAKE, 5, *GRID, FAKE, 0, -2, None) == -1
 
@@ -89,6 +89,7 @@ def test_cutoff_rejects_on_host():
     assert lib.cp_cutoff(FAKE, n, *GRID, c, b, 16, ws, need, FAKE, None) != -4  # would launch: no GPU here
     assert lib.cp_cutoff(FAKE, n, *GRID, c, b, 16, ws, need - 1, FAKE, None) == -4
     assert lib.cp_cutoff(FAKE, n, *GRID, c, b, 12, ws, need, FAKE, None) == -5   # capacity
+    assert lib.cp_cutoff(FAKE, n, *GRID, c, b, -8, ws, need, FAKE, None) == -5
     assert lib.cp_cutoff(FAKE, n, *GRID, -1.0, b, 16, ws, need, FAKE, None) == -1
     assert lib.cp_cutoff(FAKE, n, *GRID, c, 0.0, 16, ws, need, FAKE, None) == -1
     assert lib.cp_cutoff(FAKE, n, *GRID, c, b, 16, ctypes.c_void_p(0x100010), need, FAKE, None) == -2
@@ -137,7 +138,8 @@ def test_offset_list_runs_wellformed():
     runs = cp.offset_list((200, 200, 200), (0, 0, 0), 0.5, 12.0, 4.0)
     assert len(runs) > 0
     assert np.all(runs[:, 3] >= runs[:, 2])
-    assert np.all(runs[:, 3] - runs[:, 2] + 1 <= 8)
+    # one run per (dy, dz) row
+    assert len({(int(a), int(b)) for a, b in runs[:, :2]}) == len(runs)
     # the home bin and its face neighbours are always listed
     def listed(dx, dy, dz):
         sel = (runs[:, 0] == dy) & (runs[:, 1] == dz)

@@ -33,7 +33,7 @@ def _compare(atoms, shape, origin, h, c, b, K):
     return st
 
 
-@pytest.mark.parametrize("K", [8, 16])
+@pytest.mark.parametrize("K", [0, 8, 16])
 @pytest.mark.parametrize("seed,n,shape,h,origin,c,b", [
     (401, 3000, (24, 20, 17), 0.5, (0.0, 0.0, 0.0), 3.0, 1.0),
     (402, 5000, (19, 23, 16), 0.4, (-2.1, 0.7, 3.3), 2.5, 0.6),
@@ -55,7 +55,7 @@ def test_binning_faces_crowded_and_dropped():
         rows.append([3.2 + 0.001 * t, 2.5, 4.75, (t % 7) - 3.0])
     rows += [[np.nan, 0, 0, 1], [-1e9, 0, 0, 1], [0, 1e9, 0, 1], [np.inf, -np.inf, 0, 1]]
     atoms = np.asarray(rows, dtype=np.float32)
-    for K in (8, 16):
+    for K in (0, 8, 16):
         st = _compare(atoms, shape, origin, h, c, b, K)
         assert st["n_dropped"] == 4 and st["max_bin_count"] >= 300
 
@@ -68,5 +68,5 @@ def test_binning_zero_atoms():
 @pytest.mark.parametrize("name", ["cutoff_uniform", "cutoff_large"])
 def test_binning_workloads(name):
     w = workloads.make(name)
-    for K in (8, 16):
+    for K in (0, 8, 16):
         _compare(w.atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, K)

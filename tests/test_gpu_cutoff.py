@@ -19,7 +19,7 @@ def _run(w, c, b, K=16, **kw):
     return V
 
 
-@pytest.mark.parametrize("K", [8, 16])
+@pytest.mark.parametrize("K", [0, 8, 16])
 @pytest.mark.parametrize("seed,n,shape,h,origin,c,b", [
     (301, 1500, (24, 20, 17), 0.5, (0.0, 0.0, 0.0), 3.0, 1.0),
     (302, 900, (19, 23, 16), 0.4, (-2.1, 0.7, 3.3), 2.5, 1.3),     # bricks not aligned with bins
@@ -34,7 +34,7 @@ def test_cutoff_small_full_grid(K, seed, n, shape, h, origin, c, b):
     assert_within_bound(V.cpu().numpy(), ref, bound, w.name)
 
 
-@pytest.mark.parametrize("K", [8, 16])
+@pytest.mark.parametrize("K", [0, 8, 16])
 def test_cutoff_all_atoms_in_one_bin(K):
     """Every atom in one bin: capacity overflow for every atom past K."""
     rng = np.random.default_rng(5)

@@ -34,11 +34,22 @@ def test_direct_small_full_grid(seed, n, shape, h, origin):
     _check_full(w)
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("variant", sorted(cp.DIRECT_VARIANTS))
 @pytest.mark.parametrize("split", [1, 2, 3, 5, 8])
 def test_direct_every_variant_and_split(variant, split):
     w = workloads.random_case(200 + variant, 1537, (44, 13, 6), h=0.5, origin=(-1.0, 0.0, 2.0), margin=1.0)
     _check_full(w, variant=variant, split=split)
+
+
+@pytest.mark.parametrize("kind,bound", [("sfu", 1e-6), ("fma", 5e-6)])
+def test_rsqrt_routes_error_bound(kind, bound):
+    """Both rsqrt routes of the kernels against fp64 1/sqrt over 12 decades."""
+    rng = np.random.default_rng(17)
+    x = np.exp(rng.uniform(np.log(1e-4), np.log(1e8), 1 << 20)).astype(np.float32)
+    x = np.concatenate([x, (2.0 ** np.arange(-40, 40)).astype(np.float32)])
+    y = cp.eval_rsqrt(torch.from_numpy(x).cuda(), kind).cpu().numpy().astype(np.float64)
+    rel = np.abs(y * np.sqrt(x.astype(np.float64)) - 1.0)
+    assert rel.max() <= bound, rel.max()
 
 
 def test_direct_zero_atoms():
