@@ -417,15 +417,26 @@ def run_ours(args):
     # rooflines -------------------------------------------------------------
     f_mhz = clocks.get("sm_mhz") or 2070.0
     clock_basis = "median SM clock sampled during the timed steps" if clocks.get("sm_mhz") else "max SM clock"
-    # direct: every pair needs one MUFU rsqrt and at least two FP32 FMAs
-    per_sm_direct = min(r_mufu, r_ffma / 2.0)
-    peak_direct = per_sm_direct * n_sm * f_mhz * 1e6 * world
+    sm_clk = n_sm * f_mhz * 1e6 * world  # SM clock cycles per second, whole job
+    # direct: per pair at least 1 SFU rsqrt, 3 FP32 ops (dx, r^2, accumulate)
+    # and 4 issue slots: pairs/clk/SM = min(R_sfu, R_fp32/3, 128/4)
+    per_sm_direct = min(r_mufu, r_ffma / 3.0, 32.0)
+    peak_direct = per_sm_direct * sm_clk
     achieved_direct = direct_rate
-    # cutoff: a useful pair needs one MUFU rsqrt and about 8 issue slots
-    # (dx, r^2, compare, two polynomial FMAs, subtract, accumulate + MUFU issue)
-    per_sm_useful = min(r_mufu, 128.0 / 8.0, r_ffma / 7.0)
+    # the same pair with its rsqrt split between the SFU and the FMA pipe
+    # (estimate + two Newton steps: 7 FP32 ops): best split f solves
+    # (1 - f)/R_sfu = (3 + 7f)/R_fp32
+    f_split = (r_ffma - 3.0 * r_mufu) / (r_ffma + 7.0 * r_mufu)
+    per_sm_split = r_mufu / (1.0 - f_split)
+    # cutoff: a useful pair needs 1 SFU rsqrt and about 11 FP32 ops (dx, dy,
+    # dz, three for r^2, compare, two for g, subtract, accumulate):
+    # useful pairs/clk/SM = min(R_sfu, R_fp32/11)
+    per_sm_useful = min(r_mufu, r_ffma / 11.0)
     useful_rate = counts["useful"] * world * K / t_map
-    peak_useful = per_sm_useful * n_sm * f_mhz * 1e6 * world
+    peak_useful = per_sm_useful * sm_clk
+    # tighter: with dy, dz and the row sums amortised over a thread's points,
+    # 8 issue slots and one SFU op per useful pair: min(R_sfu, 128/8)
+    per_sm_useful_tight = min(r_mufu, 16.0)
     # binning: HBM bytes it must move at least (atoms in, bin-sorted atoms and
     # indices out, counts and starts, fixed-capacity slots out)
     L = cp.cutoff_layout(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity)
@@ -491,8 +502,12 @@ def run_ours(args):
             "unit": "pair evals/s",
             "frac": achieved_direct / peak_direct,
             "traffic": traffic,
-            "peak_basis": f"{n_sm} SMs x {per_sm_direct:.2f} pairs/clk/SM (measured MUFU rsqrt "
-                          f"{r_mufu:.2f}/clk/SM, FFMA {r_ffma:.1f}/clk/SM) x {f_mhz:.0f} MHz ({clock_basis})",
+            "peak_basis": f"{n_sm} SMs x {per_sm_direct:.2f} pairs/clk/SM = min(SFU rsqrt {r_mufu:.2f}, "
+                          f"FFMA {r_ffma:.1f}/3, issue 128/4) measured per SM clock, x {f_mhz:.0f} MHz ({clock_basis})",
+            "peak_split_rsqrt": per_sm_split * sm_clk,
+            "frac_split_rsqrt": achieved_direct / (per_sm_split * sm_clk),
+            "split_basis": f"rsqrt shared between SFU and FMA pipe at the best share {f_split:.2f}: "
+                           f"{per_sm_split:.1f} pairs/clk/SM",
         },
         "direct": {
             "pair_evals_per_s": direct_rate,
@@ -513,7 +528,10 @@ def run_ours(args):
                 "achieved": useful_rate, "peak": peak_useful, "unit": "useful pair evals/s",
                 "frac": useful_rate / peak_useful,
                 "time_vs_useful_pair_roofline": peak_useful / useful_rate if useful_rate > 0 else None,
-                "peak_basis": f"{n_sm} SMs x {per_sm_useful:.2f} useful pairs/clk/SM x {f_mhz:.0f} MHz",
+                "peak_basis": f"{n_sm} SMs x {per_sm_useful:.2f} useful pairs/clk/SM = min(SFU {r_mufu:.2f}, "
+                              f"FFMA {r_ffma:.1f}/11) x {f_mhz:.0f} MHz",
+                "time_vs_tight_bound": per_sm_useful_tight * sm_clk / useful_rate if useful_rate > 0 else None,
+                "tight_basis": f"min(SFU {r_mufu:.2f}, 128 issue/8) = {per_sm_useful_tight:.1f} useful pairs/clk/SM",
             },
             "roofline_binning": {
                 "bound": "hbm", "achieved": bin_bytes * world * K / t_bin / 1e9, "peak": hbm_peak, "unit": "GB/s",

@@ -29,6 +29,7 @@ __all__ = [
     "direct",
     "cutoff",
     "cutoff_workspace_bytes",
+    "direct_plan",
     "cutoff_layout",
     "bin_atoms",
     "cutoff_stats",
@@ -143,6 +144,14 @@ def direct(atoms, shape, origin, h, out=None, stream=None, variant: int = -1, sp
                                   int(variant), int(split), s)
     _check(rc, "cp_direct")
     return _finish_host(V, host_out) if on_host else V
+
+
+def direct_plan(n_atoms, shape) -> tuple:
+    """(variant, split) that cp_direct picks for this grid and atom count on the current GPU."""
+    v, sp = ctypes.c_int(0), ctypes.c_int(0)
+    nx, ny, nz = (int(x) for x in shape)
+    _check(library().cp_direct_plan(int(n_atoms), nx, ny, nz, ctypes.byref(v), ctypes.byref(sp)), "cp_direct_plan")
+    return int(v.value), int(sp.value)
 
 
 def cutoff_layout(n_atoms, shape, origin, h, cutoff, bin_size, capacity: int = 16):

@@ -265,13 +265,24 @@ __device__ __forceinline__ int brick_home_dev(int brick, int m, double h, double
 
 // Atoms per shared-memory stage.  The producer packs as many bin runs (or
 // pieces of runs) into a stage as fit, so a stage usually holds several
-// runs and a consumer warp synchronises once per stage, not once per run.
-constexpr int kStageAtoms = 128;
+// runs and the consumers synchronise once per stage, not once per run.
+// Each consumer warp sorts one 32-atom quarter of a stage into the lists.
+constexpr int kWarpSlots = 32;
+constexpr int kStageAtoms = kWarpSlots * kBrickConsumerWarps;
+
+// Barrier among the consumer warps only (the producer warp keeps streaming).
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kBrickConsumerWarps) : "memory");
+}
 
 template <int K, bool VEC, bool COUNT>
 __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __grid_constant__ BrickParams p) {
     __shared__ __align__(128) float4 ring[kBrickStages][kStageAtoms];
-    __shared__ __align__(16) AtomPair wlist[kBrickConsumerWarps][kStageAtoms];
+    // list b (atoms that can reach sub-box b) in segments, one per writing
+    // warp, so that list order never depends on timing
+    __shared__ __align__(16) AtomPair wlist[kBrickConsumerWarps][kBrickConsumerWarps][kWarpSlots];
+    __shared__ int wcount[kBrickConsumerWarps][kBrickConsumerWarps];
+    __shared__ volatile int abort_flag;
     __shared__ uint64_t full[kBrickStages], empty[kBrickStages];
     __shared__ volatile int stage_n[kBrickStages];
 
@@ -286,6 +297,7 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kBrickConsumerWarps);
         }
+        abort_flag = 0;
         mbar_init_fence();
     }
     __syncthreads();
@@ -405,7 +417,8 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
     // ---------------------------------------------------------------- consumers
     // A lane owns 4 consecutive x points (two f32x2 pairs) of one y row and z
     // plane: x = 8bx + xq .. +3, y = 8by + yy, z = 8bz + zz.  Warp w covers
-    // an 8 x 4 x 4-point sub-box of the brick.
+    // sub-box w of the brick: all 8 x, y rows 4*(w & 1) .. +3, z planes
+    // 4*(w >> 1) .. +3.
     const int xq = (lane & 1) * 4;
     const int yy = (warp & 1) * 4 + ((lane >> 1) & 3);
     const int zz = (warp >> 1) * 4 + (lane >> 3);
@@ -417,83 +430,93 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
     const float2 Y2 = make_float2(y, y), Z2 = make_float2(z, z);
     const float2 NG0 = make_float2(-p.gc0, -p.gc0), NG1 = make_float2(-p.gc1, -p.gc1);
     const float2 NG2 = make_float2(-p.gc2, -p.gc2);
-    // the warp's sub-box, from the same coordinate formula as the points
+    // the four sub-boxes share their x extent; two y and two z extents
     const float lox = fmaf((float)(kBrick * bx), p.h, p.ox), hix = fmaf((float)(kBrick * bx + 7), p.h, p.ox);
-    const int jb = kBrick * by + (warp & 1) * 4, kb = kBrick * bz + (warp >> 1) * 4;
-    const float loy = fmaf((float)jb, p.h, p.oy), hiy = fmaf((float)(jb + 3), p.h, p.oy);
-    const float loz = fmaf((float)kb, p.h, p.oz), hiz = fmaf((float)(kb + 3), p.h, p.oz);
-    AtomPair *list = wlist[warp];
+    const float loy0 = fmaf((float)(kBrick * by), p.h, p.oy), hiy0 = fmaf((float)(kBrick * by + 3), p.h, p.oy);
+    const float loy1 = fmaf((float)(kBrick * by + 4), p.h, p.oy), hiy1 = fmaf((float)(kBrick * by + 7), p.h, p.oy);
+    const float loz0 = fmaf((float)(kBrick * bz), p.h, p.oz), hiz0 = fmaf((float)(kBrick * bz + 3), p.h, p.oz);
+    const float loz1 = fmaf((float)(kBrick * bz + 4), p.h, p.oz), hiz1 = fmaf((float)(kBrick * bz + 7), p.h, p.oz);
+    const unsigned below = (1u << lane) - 1u;
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     unsigned long long n_real = 0, n_near = 0, n_useful = 0;  // COUNT only
     for (int seq = 0;; ++seq) {
         const int s = seq % kBrickStages;
-        if (!mbar_wait(&full[s], (uint32_t)((seq / kBrickStages) & 1), p.status)) break;
-        const int n = stage_n[s];
-        if (n < 0) break;
-        // (1) keep the atoms that can reach a point of this warp's sub-box:
-        // 32 slots per step, compacted into the warp's list (each component
-        // stored twice, coordinates negated, for the f32x2 pair loop)
-        const float4 *slots = &ring[s][0];
-        int cnt = 0;  // atoms listed for this warp
-        for (int base = 0; base < n; base += 32) {
-            bool near = false;
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (base + lane < n) {
-                a = slots[base + lane];
-                const float ex = fmaxf(fmaxf(lox - a.x, a.x - hix), 0.0f);
-                const float ey = fmaxf(fmaxf(loy - a.y, a.y - hiy), 0.0f);
-                const float ez = fmaxf(fmaxf(loz - a.z, a.z - hiz), 0.0f);
-                near = fmaf(ex, ex, fmaf(ey, ey, ez * ez)) < p.cull2;
-                if (COUNT && a.x < 1.0e17f) ++n_real;
-            }
-            const unsigned mask = __ballot_sync(0xffffffffu, near);
-            if (near) {
-                const int pos = cnt + __popc(mask & ((1u << lane) - 1u));
-                list[pos] = AtomPair{make_float2(-a.x, -a.x), make_float2(-a.y, -a.y), make_float2(-a.z, -a.z),
-                                     make_float2(a.w, a.w)};
-            }
-            cnt += __popc(mask);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);  // the stage is free again
-        if (COUNT) n_near += (unsigned)cnt;
-        // (2) every listed atom against the lane's 4 points
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-        for (int t = 0; t < cnt; ++t) {
-            const AtomPair a = list[t];  // broadcast
-            const float2 dy = __fadd2_rn(Y2, a.y);
-            const float2 dz = __fadd2_rn(Z2, a.z);
-            const float2 dyz2 = __ffma2_rn(dy, dy, __fmul2_rn(dz, dz));
-            const float2 dx01 = __fadd2_rn(X01, a.x);
-            const float2 dx23 = __fadd2_rn(X23, a.x);
-            const float2 r01 = __ffma2_rn(dx01, dx01, dyz2);
-            const float2 r23 = __ffma2_rn(dx23, dx23, dyz2);
-            // e = rsqrt(r^2) - g(r^2), with -g by Horner on the negated coefficients
-            const float2 rs01 = make_float2(sfu_rsqrt(r01.x), sfu_rsqrt(r01.y));
-            const float2 rs23 = make_float2(sfu_rsqrt(r23.x), sfu_rsqrt(r23.y));
-            const float2 e01 = __fadd2_rn(rs01, __ffma2_rn(__ffma2_rn(r01, NG2, NG1), r01, NG0));
-            const float2 e23 = __fadd2_rn(rs23, __ffma2_rn(__ffma2_rn(r23, NG2, NG1), r23, NG0));
-            if (r01.x < p.c2) part[0] = fmaf(a.q.x, e01.x, part[0]);
-            if (r01.y < p.c2) part[1] = fmaf(a.q.x, e01.y, part[1]);
-            if (r23.x < p.c2) part[2] = fmaf(a.q.x, e23.x, part[2]);
-            if (r23.y < p.c2) part[3] = fmaf(a.q.x, e23.y, part[3]);
-            if (COUNT) {
-                const float r2c[4] = {r01.x, r01.y, r23.x, r23.y};
+        const bool got = mbar_wait(&full[s], (uint32_t)((seq / kBrickStages) & 1), p.status);
+        if (!got) abort_flag = 1;
+        const int n = got ? stage_n[s] : -1;
+        if (n >= 0) {
+            // (1) this warp's quarter of the stage against all four sub-boxes;
+            // an atom that can reach sub-box b is appended to segment `warp`
+            // of list b (each component stored twice, coordinates negated)
+            const int i = kWarpSlots * warp + lane;
+            const bool valid = i < n;
+            const float4 a = valid ? ring[s][i] : make_float4(kPadCoord, kPadCoord, kPadCoord, 0.f);
+            if (COUNT && valid && a.x < 1.0e17f) ++n_real;
+            const float ex = fmaxf(fmaxf(lox - a.x, a.x - hix), 0.0f);
+            const float ey0 = fmaxf(fmaxf(loy0 - a.y, a.y - hiy0), 0.0f);
+            const float ey1 = fmaxf(fmaxf(loy1 - a.y, a.y - hiy1), 0.0f);
+            const float ez0 = fmaxf(fmaxf(loz0 - a.z, a.z - hiz0), 0.0f);
+            const float ez1 = fmaxf(fmaxf(loz1 - a.z, a.z - hiz1), 0.0f);
+            const float e2y0 = fmaf(ey0, ey0, ex * ex), e2y1 = fmaf(ey1, ey1, ex * ex);
+            const AtomPair e = AtomPair{make_float2(-a.x, -a.x), make_float2(-a.y, -a.y), make_float2(-a.z, -a.z),
+                                        make_float2(a.w, a.w)};
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    if (r2c[c] < p.c2 && i0 + c < p.nx && j < p.ny && k < p.nz) ++n_useful;
+            for (int b = 0; b < kBrickConsumerWarps; ++b) {
+                const float ez = (b >> 1) ? ez1 : ez0;
+                const bool near = fmaf(ez, ez, (b & 1) ? e2y1 : e2y0) < p.cull2;
+                const unsigned m = __ballot_sync(0xffffffffu, near);
+                if (near) wlist[b][warp][__popc(m & below)] = e;
+                if (lane == 0) wcount[b][warp] = __popc(m);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+        }
+        consumer_sync();  // every list segment of this stage is written
+        if (abort_flag || n < 0) break;
+        // (2) every atom listed for this warp's sub-box against the lane's 4 points
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int g = 0; g < kBrickConsumerWarps; ++g) {
+            const int cnt = wcount[warp][g];
+            if (COUNT) n_near += (unsigned)cnt;
+            const AtomPair *list = &wlist[warp][g][0];
+#pragma unroll 2
+            for (int t = 0; t < cnt; ++t) {
+                const AtomPair a = list[t];  // broadcast
+                const float2 dy = __fadd2_rn(Y2, a.y);
+                const float2 dz = __fadd2_rn(Z2, a.z);
+                const float2 dyz2 = __ffma2_rn(dy, dy, __fmul2_rn(dz, dz));
+                const float2 dx01 = __fadd2_rn(X01, a.x);
+                const float2 dx23 = __fadd2_rn(X23, a.x);
+                const float2 r01 = __ffma2_rn(dx01, dx01, dyz2);
+                const float2 r23 = __ffma2_rn(dx23, dx23, dyz2);
+                // e = rsqrt(r^2) - g(r^2), with -g by Horner on the negated coefficients
+                const float2 rs01 = make_float2(sfu_rsqrt(r01.x), sfu_rsqrt(r01.y));
+                const float2 rs23 = make_float2(sfu_rsqrt(r23.x), sfu_rsqrt(r23.y));
+                const float2 e01 = __fadd2_rn(rs01, __ffma2_rn(__ffma2_rn(r01, NG2, NG1), r01, NG0));
+                const float2 e23 = __fadd2_rn(rs23, __ffma2_rn(__ffma2_rn(r23, NG2, NG1), r23, NG0));
+                if (r01.x < p.c2) part[0] = fmaf(a.q.x, e01.x, part[0]);
+                if (r01.y < p.c2) part[1] = fmaf(a.q.x, e01.y, part[1]);
+                if (r23.x < p.c2) part[2] = fmaf(a.q.x, e23.x, part[2]);
+                if (r23.y < p.c2) part[3] = fmaf(a.q.x, e23.y, part[3]);
+                if (COUNT) {
+                    const float r2c[4] = {r01.x, r01.y, r23.x, r23.y};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (r2c[c] < p.c2 && i0 + c < p.nx && j < p.ny && k < p.nz) ++n_useful;
+                }
             }
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[c] += part[c];
-        __syncwarp();  // the list is rewritten by the next stage
+        consumer_sync();  // the lists are rewritten by the next stage
     }
 
     if (COUNT) {
-        // per warp: real atoms seen and atoms listed, each examined against
-        // the warp's 128 points; useful = pairs with r < c at stored points
+        // per warp: atoms listed for its sub-box, each evaluated against the
+        // warp's 128 points; real atoms it sorted; useful = pairs with r < c
+        // at stored points
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             n_real += __shfl_down_sync(0xffffffffu, n_real, o);
@@ -502,7 +525,8 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
         if (lane == 0) {
             atomicAdd(&p.counts[0], n_useful);
             atomicAdd(&p.counts[1], n_near * 128ull);
-            atomicAdd(&p.counts[2], n_real * 128ull);
+            // each real atom a lane sorted was examined against all 512 points
+            atomicAdd(&p.counts[2], n_real * 128ull * kBrickConsumerWarps);
         }
         return;
     }

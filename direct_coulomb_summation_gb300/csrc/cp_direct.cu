@@ -43,10 +43,15 @@ namespace cpmap {
 constexpr int kDirectThreads = 128;
 constexpr int kDirectTile = 256;  // atoms per shared-memory stage (4 KiB as loaded)
 constexpr int kDirectStages = 3;
-// dynamic shared memory: the TMA ring of raw atoms, then the expanded tile
-// (each atom as (-x,-x), (-y,-y), (-z,-z), (q,q): 32 bytes)
+// dynamic shared memory: the TMA ring of raw atoms, the expanded tile (each
+// atom as (-x,-x), (-y,-y), (-z,-z), (q,q): 32 bytes), then every thread's
+// running totals (up to 16 point pairs of 8 bytes)
 constexpr int kDirectRingBytes = kDirectStages * kDirectTile * 16;
-constexpr int kDirectSmem = kDirectRingBytes + kDirectTile * 32;
+constexpr int kDirectTileBytes = kDirectTile * 32;
+constexpr int kDirectMaxPairs = 16;
+constexpr int direct_smem_bytes(int py, int pz) {
+    return kDirectRingBytes + kDirectTileBytes + kDirectThreads * (2 * py * pz) * 8;
+}
 constexpr int kMaxSplit = 8;  // portable cluster size
 
 struct DirectParams {
@@ -91,6 +96,7 @@ template <int PY, int PZ, int EMU, bool VEC>
 __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_constant__ DirectParams p) {
     constexpr int NP = 2 * PY * PZ;  // point pairs per thread
     static_assert(EMU >= 0 && EMU <= NP, "EMU counts point pairs");
+    static_assert(NP <= kDirectMaxPairs, "running totals do not fit");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[kDirectStages];
     float4 *ring = reinterpret_cast<float4 *>(smem);
@@ -146,10 +152,12 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
         for (int s = 0; s < kDirectStages && s < n_tiles; ++s) issue(s, s);
     }
 
-    // acc[(k*PY + j)*2 + h]: pair h (points 0,1 or 2,3) of row j, plane k
-    float2 acc[NP];
+    // Pair q = (k*PY + j)*2 + h is points (0,1) or (2,3) of row j, plane k.
+    // Each tile is summed in registers (part); the running totals stay in
+    // shared memory (tot[q][tid]), which keeps registers for the pair loop.
+    float2 *tot = reinterpret_cast<float2 *>(smem + kDirectRingBytes + kDirectTileBytes);
 #pragma unroll
-    for (int q = 0; q < NP; ++q) acc[q] = make_float2(0.f, 0.f);
+    for (int q = 0; q < NP; ++q) tot[q * kDirectThreads + tid] = make_float2(0.f, 0.f);
 
     for (int it = 0; it < n_tiles; ++it) {
         const int stage = it % kDirectStages;
@@ -202,10 +210,13 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
             }
         }
 #pragma unroll
-        for (int q = 0; q < NP; ++q) acc[q] = __fadd2_rn(acc[q], part[q]);
+        for (int q = 0; q < NP; ++q) tot[q * kDirectThreads + tid] = __fadd2_rn(tot[q * kDirectThreads + tid], part[q]);
         __syncthreads();  // every thread is done with the expanded tile
     }
 
+    float2 acc[NP];
+#pragma unroll
+    for (int q = 0; q < NP; ++q) acc[q] = tot[q * kDirectThreads + tid];
     if (split == 1) {
         if (patch < p.npatch) {
 #pragma unroll
@@ -219,10 +230,12 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
         return;
     }
 
-    // Cluster reduction: partials in this CTA's shared memory (the ring is
-    // free: the last stage was consumed before the final __syncthreads),
-    // summed over ranks 0..S-1 in order by the CTA that owns each element.
+    // Cluster reduction: partials in this CTA's shared memory (the ring and
+    // the tile are free: the last tile was consumed before the final
+    // __syncthreads), summed over ranks 0..S-1 in order by the CTA that owns
+    // each element.
     constexpr int R = PY * PZ;
+    static_assert(R * kDirectThreads * 16 <= kDirectRingBytes + kDirectTileBytes, "partials do not fit");
     float4 *partial = ring;  // [R][kDirectThreads] float4
 #pragma unroll
     for (int k = 0; k < PZ; ++k)
@@ -265,15 +278,21 @@ namespace {
 
 using KernelFn = void (*)(DirectParams);
 
+// Patch shapes.  `rate` is the pair rate per SM clock each one reached on a
+// GB300 at full occupancy (128x128x64 and 200^3 grids, 40k and 100k atoms);
+// the planner uses it to rank the shapes.
 struct Variant {
     int py, pz, emu;
+    double rate;
     KernelFn vec, scalar;
 };
 
-#define CP_VARIANT(PY, PZ, EMU) {PY, PZ, EMU, direct_kernel<PY, PZ, EMU, true>, direct_kernel<PY, PZ, EMU, false>}
+#define CP_VARIANT(PY, PZ, EMU, RATE) \
+    {PY, PZ, EMU, RATE, direct_kernel<PY, PZ, EMU, true>, direct_kernel<PY, PZ, EMU, false>}
 const Variant kVariants[] = {
-    CP_VARIANT(4, 2, 0), CP_VARIANT(2, 2, 0), CP_VARIANT(4, 1, 0), CP_VARIANT(2, 1, 0), CP_VARIANT(1, 1, 0),
-    CP_VARIANT(4, 2, 4), CP_VARIANT(4, 2, 5), CP_VARIANT(2, 2, 2), CP_VARIANT(4, 1, 2), CP_VARIANT(2, 1, 1),
+    CP_VARIANT(4, 2, 0, 15.3), CP_VARIANT(2, 2, 0, 15.0), CP_VARIANT(4, 1, 0, 15.0), CP_VARIANT(2, 1, 0, 14.8),
+    CP_VARIANT(1, 1, 0, 14.6), CP_VARIANT(4, 2, 4, 17.6), CP_VARIANT(4, 2, 5, 17.4), CP_VARIANT(2, 2, 2, 17.7),
+    CP_VARIANT(4, 1, 2, 17.3), CP_VARIANT(2, 1, 1, 15.6),
 };
 #undef CP_VARIANT
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
@@ -290,14 +309,15 @@ int resident_ctas(int v, int s, bool vec, const DeviceInfo &dev) {
     int slots = 0;
     if (s == 1) {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDirectThreads, kDirectSmem) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDirectThreads,
+                                                          direct_smem_bytes(kVariants[v].py, kVariants[v].pz)) != cudaSuccess)
             return -1;
         slots = per_sm * dev.sm_count;
     } else {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(s * 64, 1, 1);
         cfg.blockDim = dim3(kDirectThreads, 1, 1);
-        cfg.dynamicSmemBytes = kDirectSmem;
+        cfg.dynamicSmemBytes = direct_smem_bytes(kVariants[v].py, kVariants[v].pz);
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
         attr.val.clusterDim.x = s;
@@ -321,23 +341,15 @@ struct Plan {
     long long npatch;
 };
 
-// Modelled pairs per SM clock of a patch shape: the slowest of the SFU
-// (16 rsqrt/clk), the FMA pipe (about 125 fp32 lane operations/clk; an
-// f32x2 instruction counts two) and instruction issue (4 warp instructions,
-// i.e. 128 thread instructions, per clk), per atom and thread.
-double variant_rate(int py, int pz, int emu) {
-    const double P = 4.0 * py * pz;        // points per thread
-    const double npair = P / 2.0;          // f32x2 point pairs
-    const double sfu = P - 2.0 * emu;      // rsqrt on the SFU
-    const double issue = 2.0 + 2.0 + 2.0 * py + pz + py * pz + 2.0 * npair + sfu + 11.0 * emu + 1.0;
-    const double fma = 4.0 + 4.0 * py + 2.0 * pz + 2.0 * py * pz + 2.0 * P + 14.0 * emu;
-    const double clk = std::max(sfu / 16.0, std::max(fma / 125.0, issue / 128.0));
-    return P / clk;
-}
+// Throughput of an SM relative to full occupancy when `warps` warps are
+// resident: the pair loop needs about 24 warps per SM to hide the SFU and
+// FMA latencies.
+double occupancy_factor(double warps) { return std::sqrt(std::min(1.0, warps / 24.0)); }
 
-// Picks the patch shape and cluster split with the smallest modelled time:
-// CTA waves x the time one CTA takes while sharing its SM with the other
-// resident CTAs, plus a fixed cost per CTA.
+// Picks the patch shape and cluster split with the smallest modelled time.
+// CTAs spread evenly over the SMs; the busiest SM runs ceil(CTAs / SMs) of
+// them, at most `resident` at a time, at the shape's measured pair rate
+// scaled by its occupancy; each split level adds a small reduction cost.
 int plan_direct(const Grid &g, int n_atoms, bool vec, const DeviceInfo &dev, Plan *out) {
     double best = INFINITY;
     for (int v = 0; v < kNumVariants; ++v) {
@@ -348,17 +360,19 @@ int plan_direct(const Grid &g, int n_atoms, bool vec, const DeviceInfo &dev, Pla
         const long long npatch = qx * yb * zb;
         const long long ctas = (npatch + kDirectThreads - 1) / kDirectThreads;
         const double pts = (double)kDirectThreads * 4 * py * pz;
-        const double rate = variant_rate(py, pz, kVariants[v].emu);
         for (int s = 1; s <= kMaxSplit; ++s) {
+            if (s == 5 || s == 7) continue;
             if (s > 1 && (long long)n_atoms < (long long)s * 64) break;
             if (ctas * s > 0x7fffffffll) break;
             const int slots = resident_ctas(v, s, vec, dev);
             if (slots < 0) return CP_ERR_CUDA;
-            const double waves = std::ceil((double)(ctas * s) / slots);
-            const double per_sm = (double)slots / dev.sm_count;
-            const double atoms = std::max(1.0, (double)n_atoms / s);
-            const double t = waves * (pts * atoms * per_sm / rate + 3000.0);
-            if (t < best * 0.98) {
+            const double resident = std::max(1.0, (double)slots / dev.sm_count);
+            const double per_sm = std::ceil((double)(ctas * s) / dev.sm_count);
+            const double warps = 4.0 * std::min(per_sm, resident);
+            const double work = pts * std::max(1.0, (double)n_atoms / s);  // pairs per CTA
+            const double t = per_sm * work / (kVariants[v].rate * occupancy_factor(warps)) * (1.0 + 0.005 * s) +
+                             2000.0 * std::ceil(per_sm / resident);
+            if (t < best) {
                 best = t;
                 out->variant = v;
                 out->split = s;
@@ -416,7 +430,7 @@ int launch_direct(const float *atoms, int n_atoms, const Grid &g, float *V, cuda
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(plan.ptiles * plan.split), 1, 1);
     cfg.blockDim = dim3(kDirectThreads, 1, 1);
-    cfg.dynamicSmemBytes = kDirectSmem;
+    cfg.dynamicSmemBytes = direct_smem_bytes(kVariants[plan.variant].py, kVariants[plan.variant].pz);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -445,6 +459,22 @@ CP_API int cp_direct(const float *atoms, int n_atoms, int nx, int ny, int nz, cp
     if (n_atoms > 0 && !aligned(atoms, 16)) return CP_ERR_MISALIGNED;
     if (!aligned(V, 4)) return CP_ERR_MISALIGNED;
     return launch_direct(atoms, n_atoms, g, V, static_cast<cudaStream_t>(stream), -1, 0);
+}
+
+CP_API int cp_direct_plan(int n_atoms, int nx, int ny, int nz, int *variant, int *split) {
+    Grid g;
+    int rc = check_grid(nx, ny, nz, cp_vec3{0.f, 0.f, 0.f}, 1.0f, &g);
+    if (rc) return rc;
+    if (n_atoms < 0 || !variant || !split) return CP_ERR_INVALID_ARGUMENT;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc) return rc;
+    Plan plan;
+    rc = plan_direct(g, n_atoms, nx % 4 == 0, dev, &plan);
+    if (rc) return rc;
+    *variant = plan.variant;
+    *split = plan.split;
+    return CP_OK;
 }
 
 // Same as cp_direct with the patch shape (index into the variant table:

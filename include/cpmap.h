@@ -112,6 +112,13 @@ CP_API int cp_direct(const float *atoms, int n_atoms, int nx, int ny, int nz, cp
 CP_API int cp_direct_config(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
                             float *V, int variant, int split, void *stream);
 
+/* The patch shape (variant index as for cp_direct_config) and cluster split
+ * that cp_direct would use for this grid and atom count on the current
+ * device (assuming 16-byte aligned output).  Queries occupancy, launches
+ * nothing.  Returns CP_OK, CP_ERR_INVALID_ARGUMENT, CP_ERR_TOO_LARGE or
+ * CP_ERR_CUDA.                                                              */
+CP_API int cp_direct_plan(int n_atoms, int nx, int ny, int nz, int *variant, int *split);
+
 /* ------------------------------------------------------------------------ */
 /* Cutoff summation (Input Binning lecture, slides 24-37).
  *
