@@ -15,6 +15,9 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
                  curvature match at c), large-c limit to the direct sum plus
                  the constant shift, cdist special case, mutant detection.
   cutoff_binned  pinned: bit-identical V and pair set against cutoff_brute.
+  cutoff_hard    pinned: large-c limit equals direct exactly term by term,
+                 single-charge closed forms inside and outside c, cdist
+                 special case, mutant detection.
   bin_atoms      pinned: numpy float32 re-derivation of every bin index,
                  counts, permutation, pad layout.
 """
@@ -108,6 +111,8 @@ def _declare(lib):
     lib.or_direct.restype = _I
     lib.or_cutoff_brute.argtypes = [_P, _L, _P, _L, _I, _I, _I, _P, _F, _F, _P, _P, _I]
     lib.or_cutoff_brute.restype = _I
+    lib.or_cutoff_hard.argtypes = [_P, _L, _P, _L, _I, _I, _I, _P, _F, _F, _P, _P, _I]
+    lib.or_cutoff_hard.restype = _I
     lib.or_cutoff_binned.argtypes = [_P, _L, _P, _L, _I, _I, _I, _P, _F, _F, _F, _P, _P, _I]
     lib.or_cutoff_binned.restype = _I
     lib.or_switch_g.argtypes = [_D, _D]
@@ -191,6 +196,21 @@ def cutoff_brute(atoms, shape, origin, h, cutoff, points=None, threads: Optional
                              threads or default_threads())
     if rc != 0:
         raise ValueError(f"or_cutoff_brute failed ({rc})")
+    return V, B
+
+
+def cutoff_hard(atoms, shape, origin, h, cutoff, points=None, threads: Optional[int] = None, with_bound=True):
+    """fp64 hard-cutoff sum (no switching): sum of q/r over r^2 < c^2: (V, B)."""
+    lib = load()
+    a, p, o = _atoms(atoms), _pts(points), _origin(origin)
+    m = _npts(shape, p)
+    V = np.empty(m, dtype=np.float64)
+    B = np.empty(m, dtype=np.float64) if with_bound else None
+    rc = lib.or_cutoff_hard(_ptr(a), a.shape[0], _ptr(p), m, int(shape[0]), int(shape[1]), int(shape[2]),
+                            _ptr(o), float(np.float32(h)), float(np.float32(cutoff)), _ptr(V), _ptr(B),
+                            threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"or_cutoff_hard failed ({rc})")
     return V, B
 
 

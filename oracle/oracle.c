@@ -215,6 +215,56 @@ static void or_cutoff_range(void *vctx, long begin, long end) {
     }
 }
 
+/* Hard cutoff without switching: sum of q / r over r^2 < c^2, the form of
+ * the 27-bin kernel in PMPP ch.18 notes section 18.5. */
+typedef struct {
+    const float *atoms;
+    long n_atoms;
+    or_grid grid;
+    double c;
+    double *V, *B;
+} or_hard_ctx;
+
+static void or_hard_range(void *vctx, long begin, long end) {
+    or_hard_ctx *c = (or_hard_ctx *)vctx;
+    const double c2 = c->c * c->c;
+    for (long p = begin; p < end; ++p) {
+        double x, y, z;
+        or_point(&c->grid, p, &x, &y, &z);
+        double v = 0.0, b = 0.0;
+        for (long a = 0; a < c->n_atoms; ++a) {
+            const float *at = c->atoms + 4 * a;
+            double dx = x - (double)at[0];
+            double dy = y - (double)at[1];
+            double dz = z - (double)at[2];
+            double r2 = dx * dx + dy * dy + dz * dz;
+            if (r2 < c2) {
+                double q = (double)at[3];
+                double r = sqrt(r2);
+                v += q / r;
+                b += fabs(q) / r;
+            }
+        }
+        c->V[p] = v;
+        if (c->B) c->B[p] = b;
+    }
+}
+
+int or_cutoff_hard(const float *atoms, long n_atoms, const int *pts, long n_pts, int nx, int ny, int nz,
+                   const float *origin, float h, float cutoff, double *V, double *B, int n_threads) {
+    if (n_atoms < 0 || n_pts < 0 || !V || !(cutoff > 0.0f) || (n_atoms > 0 && !atoms)) return -1;
+    or_hard_ctx c;
+    c.atoms = atoms;
+    c.n_atoms = n_atoms;
+    c.grid = or_make_grid(pts, nx, ny, nz, origin, h);
+    c.c = (double)cutoff;
+    c.V = V;
+    c.B = B;
+    long m = pts ? n_pts : (long)nx * ny * nz;
+    or_parallel_for(m, n_threads, or_hard_range, &c);
+    return 0;
+}
+
 int or_cutoff_brute(const float *atoms, long n_atoms, const int *pts, long n_pts, int nx, int ny, int nz,
                     const float *origin, float h, float cutoff, double *V, double *B, int n_threads) {
     if (n_atoms < 0 || n_pts < 0 || !V || !(cutoff > 0.0f) || (n_atoms > 0 && !atoms)) return -1;

@@ -218,6 +218,31 @@ def pin_cutoff_large_c_limit():
     assert np.all(np.abs(vc + 15.0 / (8.0 * c) * qsum - vd) <= bound)
 
 
+def pin_hard_cutoff():
+    # closed forms: a single charge at r = sqrt(3)/4 inside c = 0.5, one at r > c outside
+    a = _atoms([[0.25, 0.25, 0.25, 1.5], [2.0, 0.0, 0.0, -1.0]])
+    V, B = oracle.cutoff_hard(a, (1, 1, 1), (0.0, 0.0, 0.0), 0.5, 0.5)
+    assert abs(V[0] - 1.5 / (SQRT3 / 4.0)) <= 1e-14 and abs(B[0] - 1.5 / (SQRT3 / 4.0)) <= 1e-14
+    # an atom exactly at r = c is excluded (strict), as in the switched sum
+    a2 = _atoms([[1.5, 2.0, 0.0, 1.0], [0.75, 1.0, 0.0, 1.0]])
+    V2, _ = oracle.cutoff_hard(a2, (1, 1, 1), (0.0, 0.0, 0.0), 0.5, 2.5)
+    assert abs(V2[0] - 1.0 / 1.25) <= 1e-15
+    # with every pair inside, the hard-cutoff sum is the direct sum (same terms, same order)
+    w = workloads.random_case(23, 130, (5, 4, 3), margin=1.5)
+    vh, _ = oracle.cutoff_hard(w.atoms, w.shape, w.origin, w.h, 1.0e4)
+    vd, _ = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+    assert np.array_equal(vh, vd)
+    # cdist special case with a finite cutoff
+    c = 1.6
+    vh, bh = oracle.cutoff_hard(w.atoms, w.shape, w.origin, w.h, c)
+    R = cdist(_coords(w.shape, w.origin, w.h), w.atoms[:, :3].astype(np.float64))
+    inside = R * R < c * c
+    q = w.atoms[:, 3].astype(np.float64)
+    assert inside.sum() > 50
+    assert np.allclose(vh, np.where(inside, 1.0 / R, 0.0) @ q, rtol=1e-12, atol=1e-12)
+    assert np.allclose(bh, np.where(inside, 1.0 / R, 0.0) @ np.abs(q), rtol=1e-12, atol=0)
+
+
 # --------------------------------------------------------------------------
 # binning and the binned route
 
@@ -316,6 +341,7 @@ PINS = {
                pin_direct_linearity, pin_direct_translation, pin_direct_point_order],
     "switch": [pin_switch_closed_forms, pin_cutoff_single_charge, pin_cutoff_strict_boundary,
                pin_cutoff_cdist, pin_cutoff_large_c_limit],
+    "hard": [pin_hard_cutoff],
     "bins": [pin_bin_rule_numpy, pin_binned_equals_brute, pin_binned_equals_brute_random],
 }
 ALL_PINS = [p for group in PINS.values() for p in group]
@@ -338,6 +364,10 @@ MUTANTS = [
      "double dy = y - (double)at[2];\n            double dz = z - (double)at[1];\n            double r = sqrt", "direct"),
     ("point_index_j_for_k", "*z = g->oz + (double)k * g->h;", "*z = g->oz + (double)j * g->h;", "direct"),
     ("bound_signed_q", "b += fabs(q) / r;", "b += q / r;", "direct"),
+    ("hard_not_strict", "            double r2 = dx * dx + dy * dy + dz * dz;\n            if (r2 < c2) {\n                double q = (double)at[3];\n                double r = sqrt(r2);",
+     "            double r2 = dx * dx + dy * dy + dz * dz;\n            if (r2 <= c2) {\n                double q = (double)at[3];\n                double r = sqrt(r2);", "hard"),
+    ("hard_bound_signed", "                v += q / r;\n                b += fabs(q) / r;\n            }\n        }\n        c->V[p] = v;\n        if (c->B) c->B[p] = b;\n    }\n}\n\nint or_cutoff_hard",
+     "                v += q / r;\n                b += q / r;\n            }\n        }\n        c->V[p] = v;\n        if (c->B) c->B[p] = b;\n    }\n}\n\nint or_cutoff_hard", "hard"),
     ("switch_coef_gc1", "(5.0 / 4.0) * s", "(5.0 / 8.0) * s", "switch"),
     ("switch_coef_gc2", "(3.0 / 8.0) * s * s", "(3.0 / 4.0) * s * s", "switch"),
     ("switch_sign", "return 1.0 / sqrt(r2) - or_switch_g(r2, c);", "return 1.0 / sqrt(r2) + or_switch_g(r2, c);", "switch"),
