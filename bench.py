@@ -568,6 +568,79 @@ def run_ours(args):
     return 0
 
 
+def run_compare(args):
+    """The pwwt.cn chapter-18 article's five-way comparison on its own case
+    (z-index 10 plane of a 100x100x50 grid at 0.5 A, 10 000 atoms): the
+    sequential CPU sum (the fp64 oracle on one core), the GPU scatter, gather,
+    coarsened and coarsened + coalesced kernels, and this library's direct
+    kernel; plus the notes' 27-bin hard-cutoff kernel against the brick map on
+    the 200^3 / 100k-atom cutoff workload.  3 warm-ups and 10 timed runs each,
+    L2 flushed before every run, CUDA events; one JSON line."""
+    import torch
+
+    import direct_coulomb_summation_gb300 as cp
+    import oracle
+    import workloads
+
+    rank, world, local = env_rank()
+    if rank != 0:
+        return 0
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def timed(fn, reps=10, warm=3):
+        for _ in range(warm):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(3)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.mean(ts)), float(np.median(ts))
+
+    w = workloads.make("direct_plane")
+    a = torch.from_numpy(w.atoms).to(device)
+    V = torch.empty((w.shape[2], w.shape[1], w.shape[0]), dtype=torch.float32, device=device)
+    t0 = time.perf_counter()
+    oracle.direct(w.atoms, w.shape, w.origin, w.h, threads=1, with_bound=False)
+    seq_ms = 1e3 * (time.perf_counter() - t0)
+    res = {"sequential (fp64 oracle, 1 core)": {"ms": seq_ms}}
+    for name in ("scatter", "gather", "coarsen", "coalesce"):
+        mean, med = timed(lambda: cp.direct_variant(name, a, w.shape, w.origin, w.h, out=V))
+        res[f"gpu {name}"] = {"ms": mean, "ms_median": med}
+    mean, med = timed(lambda: cp.direct(a, w.shape, w.origin, w.h, out=V))
+    res["gpu cp_direct (this library)"] = {"ms": mean, "ms_median": med}
+    for v in res.values():
+        v["pair_evals_per_s"] = w.n_pairs / (v["ms"] * 1e-3)
+        v["speedup_vs_sequential"] = seq_ms / v["ms"]
+
+    wc = workloads.make(CUTOFF_WL)
+    ac = torch.from_numpy(wc.atoms).to(device)
+    Vc = torch.empty((wc.shape[2], wc.shape[1], wc.shape[0]), dtype=torch.float32, device=device)
+    ws = torch.empty(max(cp.cutoff_workspace_bytes(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, 0),
+                         int(cp.library().cp_cutoff27_workspace_bytes(wc.n_atoms, *cp._grid(wc.shape, wc.origin, wc.h),
+                                                                      float(wc.cutoff)))),
+                     dtype=torch.uint8, device=device)
+    cut = {}
+    mean, med = timed(lambda: cp.cutoff27(ac, wc.shape, wc.origin, wc.h, wc.cutoff, workspace=ws, out=Vc))
+    cut["27-bin hard cutoff (bins of edge c, one thread per point)"] = {"ms": mean, "ms_median": med}
+    mean, med = timed(lambda: cp.cutoff(ac, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, 0, workspace=ws,
+                                        out=Vc))
+    cut["brick map with switched term (this library, binning included)"] = {"ms": mean, "ms_median": med}
+    for v in cut.values():
+        v["grid_points_per_s"] = wc.n_points / (v["ms"] * 1e-3)
+    print(json.dumps({"compare": "strategies of the pages on their own workloads", "device": torch.cuda.get_device_name(),
+                      "direct_workload": w.description, "direct": res,
+                      "cutoff_workload": wc.description, "cutoff": cut,
+                      "protocol": "3 warm-ups, 10 timed runs, 256 MiB L2 flush before each, CUDA events"}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -579,6 +652,8 @@ def main(argv=None):
     ap.add_argument("--only", choices=["both", "direct", "cutoff"], default="both",
                     help="time one leg only (for profiling; the JSON line then covers that leg)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--compare", action="store_true",
+                    help="time the pages' own strategies against this library (one JSON line) and exit")
     ap.add_argument("--capacity", type=int, choices=[0, 8, 16], default=CAPACITY_DEFAULT,
                     help="bin capacity of the cutoff leg (0 = contiguous bin-sorted runs, no fixed slots)")
     args = ap.parse_args(argv)
@@ -586,6 +661,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.compare:
+        return run_compare(args)
     return run_ours(args)
 
 

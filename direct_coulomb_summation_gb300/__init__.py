@@ -30,6 +30,9 @@ __all__ = [
     "cutoff",
     "cutoff_workspace_bytes",
     "direct_plan",
+    "direct_variant",
+    "cutoff27",
+    "DIRECT_STRATEGIES",
     "cutoff_layout",
     "bin_atoms",
     "cutoff_stats",
@@ -152,6 +155,38 @@ def direct_plan(n_atoms, shape) -> tuple:
     nx, ny, nz = (int(x) for x in shape)
     _check(library().cp_direct_plan(int(n_atoms), nx, ny, nz, ctypes.byref(v), ctypes.byref(sp)), "cp_direct_plan")
     return int(v.value), int(sp.value)
+
+
+DIRECT_STRATEGIES = {"scatter": 0, "gather": 1, "coarsen": 2, "coalesce": 3}
+
+
+def direct_variant(strategy: str, atoms, shape, origin, h, out=None, stream=None):
+    """The direct map by one of the pages' strategies (comparison kernels):
+    "scatter", "gather", "coarsen" or "coalesce".  Device atoms only."""
+    lib = library()
+    dev_atoms, on_host = _as_device_atoms(atoms)
+    V = _out_tensor(out, shape, dev_atoms.device)
+    n = int(dev_atoms.shape[0])
+    rc = lib.cp_direct_variant(DIRECT_STRATEGIES[strategy], dev_atoms.data_ptr() if n else None, n,
+                               *_grid(shape, origin, h), V.data_ptr(), _stream(stream))
+    _check(rc, "cp_direct_variant")
+    return _finish_host(V) if on_host else V
+
+
+def cutoff27(atoms, shape, origin, h, cutoff, workspace=None, out=None, stream=None):
+    """Hard-cutoff map (sum of q/r over r < c) by the 27-bin kernel (comparison kernel)."""
+    lib = library()
+    dev_atoms, on_host = _as_device_atoms(atoms)
+    n = int(dev_atoms.shape[0])
+    need = int(lib.cp_cutoff27_workspace_bytes(n, *_grid(shape, origin, h), float(np.float32(cutoff))))
+    if need == 0:
+        raise CpError(-1, "cp_cutoff27_workspace_bytes")
+    ws = _workspace(workspace, need, dev_atoms.device)
+    V = _out_tensor(out, shape, dev_atoms.device)
+    rc = lib.cp_cutoff27(dev_atoms.data_ptr() if n else None, n, *_grid(shape, origin, h), float(np.float32(cutoff)),
+                         ws.data_ptr(), ws.numel() * ws.element_size(), V.data_ptr(), _stream(stream))
+    _check(rc, "cp_cutoff27")
+    return _finish_host(V) if on_host else V
 
 
 def cutoff_layout(n_atoms, shape, origin, h, cutoff, bin_size, capacity: int = 16):

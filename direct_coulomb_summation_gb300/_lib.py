@@ -69,6 +69,9 @@ SIGNATURES = {
     "cp_status_string": (ctypes.c_char_p, [_I]),
     "cp_version": (_I, []),
     "cp_eval_rsqrt": (_I, [_I, _P, _P, _I, _P]),
+    "cp_direct_variant": (_I, [_I, _P, _I, *_GRID, _P, _P]),
+    "cp_cutoff27_workspace_bytes": (_SZ, [_I, *_GRID, _F]),
+    "cp_cutoff27": (_I, [_P, _I, *_GRID, _F, _P, _SZ, _P, _P]),
     "cp_probe_pipe_rate": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _P]),
 }
 

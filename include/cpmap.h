@@ -281,6 +281,36 @@ CP_API int cp_brick_home(int nx, int ny, int nz, cp_vec3 origin, float h, float 
                          int by, int bz, int home_out[3]);
 
 /* ------------------------------------------------------------------------ */
+/* Comparison kernels: the strategies the pages describe, rebuilt as plain
+ * CUDA so the optimised path can be timed against them (the pwwt.cn
+ * chapter-18 article's five-way benchmark; PMPP ch.18 notes sections
+ * 18.2-18.5).  Not the fast path.
+ *
+ * cp_direct_variant computes the same map as cp_direct with
+ *   variant 0  scatter: one thread per atom, atomicAdd into every grid point
+ *              (notes 18.2; article 二).  V is zeroed first; the summation
+ *              order depends on timing, so results vary in the last bits.
+ *   variant 1  gather: one thread per point, atoms through __constant__
+ *              memory in chunks of 4000, one launch per chunk (notes 18.2).
+ *   variant 2  coarsened gather: 4 adjacent x points per thread (notes 18.3).
+ *   variant 3  coarsened + coalesced: 4 points a block-width apart (article 三).
+ * Variants 1-3 share one __constant__ chunk table per device: calls that
+ * overlap on the GPU race.  nz <= 65535.  Same errors as cp_direct, plus
+ * CP_ERR_INVALID_ARGUMENT for an unknown variant.                           */
+CP_API int cp_direct_variant(int variant, const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin,
+                             float h, float *V, void *stream);
+
+/* The 27-bin hard-cutoff map of notes 18.5: bins of edge c; each point scans
+ * its own bin and the 26 around it and adds q/r for r^2 < c^2 (no
+ * switching).  Binning is cp_bin_atoms with bin size c and capacity 0 in a
+ * caller-owned workspace of cp_cutoff27_workspace_bytes bytes.  nz <= 65535.
+ * Same errors as cp_cutoff.                                                 */
+CP_API size_t cp_cutoff27_workspace_bytes(int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                                          float cutoff);
+CP_API int cp_cutoff27(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                       float cutoff, void *workspace, size_t workspace_bytes, float *V, void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status and measurement helpers. */
 
 /* Reads and clears the device status word of the current device
