@@ -399,6 +399,28 @@ def run_ours(args):
     sampler.mark_end()
     launches = lib.cp_launch_count() - launches0
     clocks = sampler.stop()
+    # the cutoff leg again as one captured CUDA graph (binning's six launches
+    # and the map replayed without per-launch host overhead)
+    t_graph_cut = None
+    if do_cutoff:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            gs = torch.cuda.current_stream().cuda_stream
+            call(lib.cp_bin_atoms(ac.data_ptr(), wc.n_atoms, *gc, *cut, ws.data_ptr(), ws_bytes, gs), "cp_bin_atoms")
+            call(lib.cp_cutoff_map(ac.data_ptr(), wc.n_atoms, *gc, *cut, ws.data_ptr(), ws_bytes, Vc.data_ptr(), gs),
+                 "cp_cutoff_map")
+        graph.replay()
+        torch.cuda.synchronize()
+        tg = []
+        for _ in range(max(3, min(args.steps, 20))):
+            flush.fill_(5)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            tg.append(e0.elapsed_time(e1))
+        t_graph_cut = float(np.mean(tg)) / 1e3
     status = cp.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status:#x} after the timed steps")
@@ -523,6 +545,7 @@ def run_ours(args):
             "ms": 1e3 * t_cut / K,
             "ms_binning": 1e3 * t_bin / K,
             "ms_map": 1e3 * t_map / K,
+            "ms_as_cuda_graph": None if t_graph_cut is None else 1e3 * t_graph_cut,
             "roofline_map": {
                 "bound": "alu", "kernel": "cutoff_brick_kernel (cp_cutoff_map)",
                 "achieved": useful_rate, "peak": peak_useful, "unit": "useful pair evals/s",

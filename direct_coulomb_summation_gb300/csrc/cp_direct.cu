@@ -52,7 +52,8 @@ constexpr int kDirectMaxPairs = 16;
 constexpr int direct_smem_bytes(int py, int pz) {
     return kDirectRingBytes + kDirectTileBytes + kDirectThreads * (2 * py * pz) * 8;
 }
-constexpr int kMaxSplit = 8;  // portable cluster size
+constexpr int kMaxSplit = 16;       // cluster sizes above 8 are non-portable
+constexpr int kPortableSplit = 8;
 
 struct DirectParams {
     const float4 *atoms;
@@ -230,13 +231,13 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
         return;
     }
 
-    // Cluster reduction: partials in this CTA's shared memory (the ring and
-    // the tile are free: the last tile was consumed before the final
-    // __syncthreads), summed over ranks 0..S-1 in order by the CTA that owns
-    // each element.
+    // Cluster reduction: each thread's partial sums replace the running
+    // totals in this CTA's shared memory (same size: a float4 per patch row),
+    // then every element is summed over ranks 0..S-1, in rank order, by the
+    // CTA that owns it.
     constexpr int R = PY * PZ;
-    static_assert(R * kDirectThreads * 16 <= kDirectRingBytes + kDirectTileBytes, "partials do not fit");
-    float4 *partial = ring;  // [R][kDirectThreads] float4
+    float4 *partial = reinterpret_cast<float4 *>(tot);  // [R][kDirectThreads]
+    __syncthreads();  // every thread has read its totals
 #pragma unroll
     for (int k = 0; k < PZ; ++k)
 #pragma unroll
@@ -297,16 +298,26 @@ const Variant kVariants[] = {
 #undef CP_VARIANT
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
-// Resident CTAs per GPU for variant v and cluster size s (cached per device).
+// Resident CTAs per GPU for variant v, store flavour and cluster size s,
+// cached per device; 0 if the device cannot run that cluster size.  For
+// sizes above 8 it also sets the non-portable cluster attribute of that
+// exact kernel, which the launch needs.
 std::mutex g_plan_mutex;
-int g_slots[64][kNumVariants][kMaxSplit + 1];
+int g_slots[64][kNumVariants][2][kMaxSplit + 1];  // [device][variant][vector stores][split]
 
 int resident_ctas(int v, int s, bool vec, const DeviceInfo &dev) {
     std::lock_guard<std::mutex> lock(g_plan_mutex);
-    int &cached = g_slots[dev.device][v][s];
+    int &cached = g_slots[dev.device][v][vec ? 1 : 0][s];
     if (cached > 0) return cached;
+    if (cached == -2) return 0;  // cluster size not available
     KernelFn fn = vec ? kVariants[v].vec : kVariants[v].scalar;
     int slots = 0;
+    if (s > kPortableSplit &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();  // not supported here: this split is never planned
+        cached = -2;
+        return 0;
+    }
     if (s == 1) {
         int per_sm = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDirectThreads,
@@ -326,10 +337,18 @@ int resident_ctas(int v, int s, bool vec, const DeviceInfo &dev) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) return -1;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            cached = -2;
+            return 0;
+        }
         slots = clusters * s;
     }
-    cached = slots > 0 ? slots : 1;
+    if (slots <= 0) {
+        cached = -2;
+        return 0;
+    }
+    cached = slots;
     return cached;
 }
 
@@ -361,11 +380,12 @@ int plan_direct(const Grid &g, int n_atoms, bool vec, const DeviceInfo &dev, Pla
         const long long ctas = (npatch + kDirectThreads - 1) / kDirectThreads;
         const double pts = (double)kDirectThreads * 4 * py * pz;
         for (int s = 1; s <= kMaxSplit; ++s) {
-            if (s == 5 || s == 7) continue;
+            if (s == 5 || s == 7 || (s > 8 && s != 12 && s != 16)) continue;
             if (s > 1 && (long long)n_atoms < (long long)s * 64) break;
             if (ctas * s > 0x7fffffffll) break;
             const int slots = resident_ctas(v, s, vec, dev);
             if (slots < 0) return CP_ERR_CUDA;
+            if (slots == 0) continue;  // cluster size not available on this device
             const double resident = std::max(1.0, (double)slots / dev.sm_count);
             const double per_sm = std::ceil((double)(ctas * s) / dev.sm_count);
             const double warps = 4.0 * std::min(per_sm, resident);
@@ -407,6 +427,11 @@ int launch_direct(const float *atoms, int n_atoms, const Grid &g, float *V, cuda
         plan.ptiles = (plan.npatch + kDirectThreads - 1) / kDirectThreads;
     }
     if (force_split >= 1 && force_split <= kMaxSplit) plan.split = force_split;
+    if (plan.split > kPortableSplit) {  // sets the non-portable cluster attribute, checks support
+        const int slots = resident_ctas(plan.variant, plan.split, vec, dev);
+        if (slots < 0) return CP_ERR_CUDA;
+        if (slots == 0) return CP_ERR_UNSUPPORTED;
+    }
 
     DirectParams p;
     p.atoms = reinterpret_cast<const float4 *>(atoms);

@@ -103,12 +103,13 @@ CP_API int cp_direct(const float *atoms, int n_atoms, int nx, int ny, int nz, cp
  * pairs the first EMU take their rsqrt on the FMA pipe instead of the SFU
  * ((PY, PZ, EMU)): 0 = (4,2,0), 1 = (2,2,0), 2 = (4,1,0), 3 = (2,1,0),
  * 4 = (1,1,0), 5 = (4,2,4), 6 = (4,2,5), 7 = (2,2,2), 8 = (4,1,2),
- * 9 = (2,1,1).  split: 0 =
- * planner's choice, else 1..8 CTAs of a cluster share one tile of points and
- * take 1/split of the atoms each (their partial sums meet in distributed
- * shared memory).  Results agree with cp_direct up to fp32 rounding order.
- * Same errors as cp_direct, plus CP_ERR_INVALID_ARGUMENT for an unknown
- * variant or split.                                                         */
+ * 9 = (2,1,1).  split: 0 = planner's choice, else 1..16 CTAs of a
+ * cluster share one tile of points and take 1/split of the atoms each
+ * (their partial sums meet in distributed shared memory; sizes above 8 use
+ * non-portable clusters).  Results agree with cp_direct up to fp32
+ * rounding order.  Same errors as cp_direct, plus CP_ERR_INVALID_ARGUMENT
+ * for an unknown variant or split and CP_ERR_UNSUPPORTED for a cluster size
+ * the device cannot run.                                                    */
 CP_API int cp_direct_config(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
                             float *V, int variant, int split, void *stream);
 
