@@ -195,3 +195,13 @@ def test_brick_home_contains_brick_origin():
             lo = float(np.float32(origin[d])) + 8 * brick[d] * float(np.float32(h))
             blo = float(bo[d]) + home[d] * float(np.float32(b))
             assert blo - 1e-4 <= lo < blo + float(np.float32(b)) + 1e-4
+
+
+def test_cutoff_rejects_huge_cutoff_to_bin_ratio():
+    lib = cp.library()
+    # more than 127 margin bins, or an offset list longer than the kernels take
+    assert lib.cp_cutoff_workspace_bytes(10, *GRID, 200.0, 1.0, 0) == 0
+    nr, nb = ctypes.c_int(0), ctypes.c_int(0)
+    assert lib.cp_offset_list(*GRID, 40.0, 1.0, None, 0, ctypes.byref(nr), ctypes.byref(nb)) == -3
+    ws = ctypes.c_void_p(0x100000)
+    assert lib.cp_cutoff(FAKE, 10, *GRID, 200.0, 1.0, 0, ws, 1 << 30, FAKE, None) == -3

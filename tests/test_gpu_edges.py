@@ -1,0 +1,72 @@
+"""Edge cases of the CUDA path at large or awkward sizes, against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import direct_coulomb_summation_gb300 as cp
+import oracle
+import workloads
+from gpu_util import assert_within_bound, flat_index, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def test_direct_many_atoms_small_grid():
+    """3 million atoms on a 24^3 grid: every cluster split slices the atom
+    array; 512 sampled points by the oracle."""
+    rng = np.random.default_rng(81)
+    shape, h, origin = (24, 24, 24), 0.5, (0.0, 0.0, 0.0)
+    n = 3_000_000
+    pos = workloads.off_lattice_uniform(rng, n, (-20.0, -20.0, -20.0), (32.0, 32.0, 32.0), origin, h)
+    atoms = np.empty((n, 4), dtype=np.float32)
+    atoms[:, :3] = pos
+    atoms[:, 3] = rng.uniform(-1, 1, n).astype(np.float32)
+    a = to_dev(atoms)
+    pts = workloads.sample_points(shape, 512, seed=82)
+    ref, bound = oracle.direct(atoms, shape, origin, h, points=pts)
+    idx = torch.from_numpy(flat_index(shape, pts)).cuda()
+    for split in (0, 1, 16):
+        V = cp.direct(a, shape, origin, h, split=split, variant=-1 if split == 0 else 7)
+        torch.cuda.synchronize()
+        assert_within_bound(V.reshape(-1)[idx].cpu().numpy(), ref, bound, f"split {split}")
+
+
+@pytest.mark.parametrize("K", [0, 8, 16])
+def test_cutoff_crowded_bins(K):
+    """400 000 atoms in a 12 A box, about 230 per 1 A bin: long per-bin
+    sorts, and every bin run split across many shared-memory stages."""
+    rng = np.random.default_rng(83)
+    shape, h, origin, c, b = (24, 24, 24), 0.5, (0.0, 0.0, 0.0), 3.0, 1.0
+    n = 400_000
+    pos = workloads.off_lattice_uniform(rng, n, (0.0, 0.0, 0.0), (12.0, 12.0, 12.0), origin, h)
+    atoms = np.empty((n, 4), dtype=np.float32)
+    atoms[:, :3] = pos
+    atoms[:, 3] = rng.uniform(-1, 1, n).astype(np.float32)
+    V = cp.cutoff(to_dev(atoms), shape, origin, h, c, b, capacity=K)
+    torch.cuda.synchronize()
+    assert cp.device_status() == 0
+    pts = workloads.sample_points(shape, 256, seed=84)
+    ref, bound = oracle.cutoff_brute(atoms, shape, origin, h, c, points=pts)
+    got = V.reshape(-1)[torch.from_numpy(flat_index(shape, pts)).cuda()].cpu().numpy()
+    assert_within_bound(got, ref, bound, f"K={K}")
+
+
+def test_concurrent_streams():
+    """Two direct maps and two cutoff maps in flight on two streams at once."""
+    w1 = workloads.random_case(85, 4000, (48, 32, 16), margin=2.0)
+    w2 = workloads.random_case(86, 3000, (40, 40, 8), h=0.4, origin=(1.0, -2.0, 0.5), margin=2.0)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    a1, a2 = to_dev(w1.atoms), to_dev(w2.atoms)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        d1 = cp.direct(a1, w1.shape, w1.origin, w1.h)
+        c1 = cp.cutoff(a1, w1.shape, w1.origin, w1.h, 3.0, 1.0)
+    with torch.cuda.stream(s2):
+        d2 = cp.direct(a2, w2.shape, w2.origin, w2.h)
+        c2 = cp.cutoff(a2, w2.shape, w2.origin, w2.h, 2.5, 1.2)
+    torch.cuda.synchronize()
+    for w, d, c, cc, bb in ((w1, d1, c1, 3.0, 1.0), (w2, d2, c2, 2.5, 1.2)):
+        ref, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+        assert_within_bound(d.cpu().numpy(), ref, bound, "direct")
+        ref, bound = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, cc)
+        assert_within_bound(c.cpu().numpy(), ref, bound, "cutoff")
