@@ -14,18 +14,24 @@
 //
 // The map (slides "Details on Small Bin Design" (30), "Tiling Atom Data"
 // (32), "GPU Thread Coarsening" (36), "GPU Thread Inner Loop" (37)): one CTA
-// per 8x8x8-point brick.  A producer warp walks the brick's neighbourhood
-// offset list (x-runs of bins, passed as a kernel parameter) and streams
-// each run's fixed-capacity slots -- then the overflow atoms of overfull
-// bins from the CSR array -- into a ring of shared-memory stages with 1-D
-// TMA bulk copies.  Four consumer warps own 4x4x... points: warp w covers an
-// 8x4x4 sub-box of the brick and each lane 4 consecutive x points.  For 32
-// slots at a time a warp tests every atom against its sub-box (distance to
-// the box < c) and keeps a ballot mask; only atoms that can reach one of
-// its points go through the pair loop, where the switched term
-// q * (rsqrt(r^2) - (GC0 + r^2 (GC1 + r^2 GC2))) is added for r^2 < c^2.
-// Pads (unused slots) sit at 1e18 A and never pass the sub-box test, which
-// replaces the lecture's stop-at-the-first-empty-slot rule.
+// per 8x8x8-point brick, a producer warp and four consumer warps.
+//   * The producer walks the brick's neighbourhood offset list (one x-run of
+//     bins per (dy, dz), passed as a kernel parameter) and packs the atoms
+//     into a ring of 128-atom shared-memory stages with 1-D TMA bulk copies:
+//     with capacity 0 each run is one contiguous range of the bin-sorted
+//     array; with capacity 8 or 16 it is the run's fixed-capacity slots
+//     (trimmed to its occupied bins), then the overflow of every bin holding
+//     more than the capacity.
+//   * Consumer warp w owns sub-box w of the brick (8 x 4 x 4 points; each
+//     lane 4 consecutive x points as two f32x2 pairs).  For every stage each
+//     consumer warp tests a quarter of the atoms against all four sub-boxes
+//     (distance to the box < c) and appends each atom to the list of every
+//     sub-box it can reach, in per-writer segments so that the order never
+//     depends on timing; after a consumer-only barrier each warp runs its
+//     own list through the pair loop, adding the switched term
+//     q * (rsqrt(r^2) - (GC0 + r^2 (GC1 + r^2 GC2))) for r^2 < c^2.
+//   * Unused fixed slots sit at 1e18 A and never pass the sub-box test,
+//     which replaces the lecture's stop-at-the-first-empty-slot rule.
 #include <cuda_runtime.h>
 
 #include <algorithm>
