@@ -15,12 +15,17 @@
 //     stores 32 consecutive float4s of a row (section 18.4 and the article's
 //     coarsen-plus-coalesce kernel, section 三);
 //   * atom tiles: instead of 4K-atom chunks in constant memory re-launched
-//     per chunk (section 18.2), one launch streams 512-atom tiles from global
+//     per chunk (section 18.2), one launch streams 256-atom tiles from global
 //     memory into a 3-stage shared-memory ring with 1-D TMA bulk copies; all
 //     threads read the same atom (a shared-memory broadcast);
-//   * accuracy: each tile's contribution is summed in a separate register
-//     and then added to the running total, so the fp32 rounding error grows
-//     like (tile + n_atoms / tile) instead of n_atoms;
+//   * f32x2: a thread's 4 x points are two register pairs, so r^2, the
+//     accumulate and the FMA-pipe rsqrt are paired Blackwell instructions;
+//   * rsqrt on two pipes: a compile-time share of each thread's point pairs
+//     takes its rsqrt on the FMA pipe (fma_rsqrt2) and the rest on the SFU,
+//     so that neither unit alone limits the pair rate;
+//   * accuracy: each tile's contribution is summed in separate registers and
+//     then added to a running total kept in shared memory, so the fp32
+//     rounding error grows like (tile + n_atoms / tile) instead of n_atoms;
 //   * small grids: when there are too few point patches to fill the GPU, S
 //     CTAs of a thread-block cluster share one tile of points and take 1/S
 //     of the atoms each; their partial sums meet in distributed shared
@@ -43,14 +48,12 @@ namespace cpmap {
 constexpr int kDirectThreads = 128;
 constexpr int kDirectTile = 256;  // atoms per shared-memory stage (4 KiB as loaded)
 constexpr int kDirectStages = 3;
-// dynamic shared memory: the TMA ring of raw atoms, the expanded tile (each
-// atom as (-x,-x), (-y,-y), (-z,-z), (q,q): 32 bytes), then every thread's
-// running totals (up to 16 point pairs of 8 bytes)
+// dynamic shared memory: the TMA ring of atoms, then every thread's running
+// totals (up to 16 point pairs of 8 bytes)
 constexpr int kDirectRingBytes = kDirectStages * kDirectTile * 16;
-constexpr int kDirectTileBytes = kDirectTile * 32;
 constexpr int kDirectMaxPairs = 16;
 constexpr int direct_smem_bytes(int py, int pz) {
-    return kDirectRingBytes + kDirectTileBytes + kDirectThreads * (2 * py * pz) * 8;
+    return kDirectRingBytes + kDirectThreads * (2 * py * pz) * 8;
 }
 constexpr int kMaxSplit = 16;       // cluster sizes above 8 are non-portable
 constexpr int kPortableSplit = 8;
@@ -68,11 +71,6 @@ struct DirectParams {
     unsigned int *status;
 };
 
-// One expanded atom: coordinates negated and every component duplicated, so
-// that point - atom and q * rsqrt are single f32x2 operations.
-struct __align__(16) DupAtom {
-    float2 x, y, z, q;
-};
 
 // Stores one x quad of row (y, z): a float4 when the row is 16-byte aligned
 // and complete, else the in-range scalars.
@@ -101,7 +99,6 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[kDirectStages];
     float4 *ring = reinterpret_cast<float4 *>(smem);
-    DupAtom *tile = reinterpret_cast<DupAtom *>(smem + kDirectRingBytes);
 
     const int tid = threadIdx.x;
     const int split = p.split;
@@ -123,19 +120,13 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
     const int yb = (int)(t % p.yb);
     const int zb = (int)(t / p.yb);
     const int i0 = 4 * qx, j0 = PY * yb, k0 = PZ * zb;
-    const float2 X01 = make_float2(fmaf((float)(i0 + 0), p.h, p.ox), fmaf((float)(i0 + 1), p.h, p.ox));
-    const float2 X23 = make_float2(fmaf((float)(i0 + 2), p.h, p.ox), fmaf((float)(i0 + 3), p.h, p.ox));
-    float2 Y[PY], Z[PZ];
+    float x[4], y[PY], z[PZ];
 #pragma unroll
-    for (int j = 0; j < PY; ++j) {
-        const float y = fmaf((float)(j0 + j), p.h, p.oy);
-        Y[j] = make_float2(y, y);
-    }
+    for (int c = 0; c < 4; ++c) x[c] = fmaf((float)(i0 + c), p.h, p.ox);
 #pragma unroll
-    for (int k = 0; k < PZ; ++k) {
-        const float z = fmaf((float)(k0 + k), p.h, p.oz);
-        Z[k] = make_float2(z, z);
-    }
+    for (int j = 0; j < PY; ++j) y[j] = fmaf((float)(j0 + j), p.h, p.oy);
+#pragma unroll
+    for (int k = 0; k < PZ; ++k) z[k] = fmaf((float)(k0 + k), p.h, p.oz);
 
     if (tid == 0) {
         for (int s = 0; s < kDirectStages; ++s) mbar_init(&full[s], 1);
@@ -156,7 +147,7 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
     // Pair q = (k*PY + j)*2 + h is points (0,1) or (2,3) of row j, plane k.
     // Each tile is summed in registers (part); the running totals stay in
     // shared memory (tot[q][tid]), which keeps registers for the pair loop.
-    float2 *tot = reinterpret_cast<float2 *>(smem + kDirectRingBytes + kDirectTileBytes);
+    float2 *tot = reinterpret_cast<float2 *>(smem + kDirectRingBytes);
 #pragma unroll
     for (int q = 0; q < NP; ++q) tot[q * kDirectThreads + tid] = make_float2(0.f, 0.f);
 
@@ -164,36 +155,35 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
         const int stage = it % kDirectStages;
         mbar_wait(&full[stage], (uint32_t)((it / kDirectStages) & 1), p.status);
         const int n = min(kDirectTile, n_local - it * kDirectTile);
-        const float4 *raw = ring + stage * kDirectTile;
-        for (int a = tid; a < n; a += kDirectThreads) {
-            const float4 v = raw[a];
-            tile[a] = DupAtom{make_float2(-v.x, -v.x), make_float2(-v.y, -v.y), make_float2(-v.z, -v.z),
-                              make_float2(v.w, v.w)};
-        }
-        __syncthreads();  // the expanded tile is ready, the raw stage is free
-        if (tid == 0 && it + kDirectStages < n_tiles) issue(it + kDirectStages, stage);
+        const float4 *tile = ring + stage * kDirectTile;
 
         float2 part[NP];
 #pragma unroll
         for (int q = 0; q < NP; ++q) part[q] = make_float2(0.f, 0.f);
 
+        // The per-atom differences are scalar FP32 operations written straight
+        // into the register pairs the f32x2 instructions read (dx for points
+        // 0,1 and 2,3; dy^2 + dz^2 duplicated per row), so only r^2, the
+        // accumulate and the FMA-pipe rsqrt run as f32x2.
 #pragma unroll 2
         for (int a = 0; a < n; ++a) {
-            const DupAtom at = tile[a];  // same address in every lane: broadcast
-            const float2 dx01 = __fadd2_rn(X01, at.x);
-            const float2 dx23 = __fadd2_rn(X23, at.x);
-            float2 dy2[PY];
+            const float4 at = tile[a];  // same address in every lane: broadcast
+            const float2 dx01 = make_float2(x[0] - at.x, x[1] - at.x);
+            const float2 dx23 = make_float2(x[2] - at.x, x[3] - at.x);
+            const float2 q2 = make_float2(at.w, at.w);
+            float dy2[PY];
 #pragma unroll
             for (int j = 0; j < PY; ++j) {
-                const float2 dy = __fadd2_rn(Y[j], at.y);
-                dy2[j] = __fmul2_rn(dy, dy);
+                const float dy = y[j] - at.y;
+                dy2[j] = dy * dy;
             }
 #pragma unroll
             for (int k = 0; k < PZ; ++k) {
-                const float2 dz = __fadd2_rn(Z[k], at.z);
+                const float dz = z[k] - at.z;
 #pragma unroll
                 for (int j = 0; j < PY; ++j) {
-                    const float2 dyz2 = __ffma2_rn(dz, dz, dy2[j]);
+                    const float d = fmaf(dz, dz, dy2[j]);
+                    const float2 dyz2 = make_float2(d, d);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int q = (k * PY + j) * 2 + hh;
@@ -205,14 +195,15 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
                         } else {
                             rs = make_float2(sfu_rsqrt(r2.x), sfu_rsqrt(r2.y));
                         }
-                        part[q] = __ffma2_rn(at.q, rs, part[q]);
+                        part[q] = __ffma2_rn(q2, rs, part[q]);
                     }
                 }
             }
         }
 #pragma unroll
         for (int q = 0; q < NP; ++q) tot[q * kDirectThreads + tid] = __fadd2_rn(tot[q * kDirectThreads + tid], part[q]);
-        __syncthreads();  // every thread is done with the expanded tile
+        __syncthreads();  // every thread is done with this stage
+        if (tid == 0 && it + kDirectStages < n_tiles) issue(it + kDirectStages, stage);
     }
 
     float2 acc[NP];
@@ -280,8 +271,8 @@ namespace {
 using KernelFn = void (*)(DirectParams);
 
 // Patch shapes.  `rate` is the pair rate per SM clock each one reached on a
-// GB300 at full occupancy (128x128x64 and 200^3 grids, 40k and 100k atoms);
-// the planner uses it to rank the shapes.
+// GB300 at full occupancy (best split on a 200^3 grid with 100k atoms, a
+// run of about 0.13 s); the planner uses it to rank the shapes.
 struct Variant {
     int py, pz, emu;
     double rate;
@@ -291,9 +282,9 @@ struct Variant {
 #define CP_VARIANT(PY, PZ, EMU, RATE) \
     {PY, PZ, EMU, RATE, direct_kernel<PY, PZ, EMU, true>, direct_kernel<PY, PZ, EMU, false>}
 const Variant kVariants[] = {
-    CP_VARIANT(4, 2, 0, 15.3), CP_VARIANT(2, 2, 0, 15.0), CP_VARIANT(4, 1, 0, 15.0), CP_VARIANT(2, 1, 0, 14.8),
-    CP_VARIANT(1, 1, 0, 14.6), CP_VARIANT(4, 2, 4, 17.6), CP_VARIANT(4, 2, 5, 17.4), CP_VARIANT(2, 2, 2, 17.7),
-    CP_VARIANT(4, 1, 2, 17.3), CP_VARIANT(2, 1, 1, 15.6),
+    CP_VARIANT(4, 2, 0, 15.5), CP_VARIANT(2, 2, 0, 15.4), CP_VARIANT(4, 1, 0, 15.4), CP_VARIANT(2, 1, 0, 15.5),
+    CP_VARIANT(1, 1, 0, 15.3), CP_VARIANT(4, 2, 4, 17.8), CP_VARIANT(4, 2, 5, 17.9), CP_VARIANT(2, 2, 2, 19.3),
+    CP_VARIANT(4, 1, 2, 19.1), CP_VARIANT(2, 1, 1, 18.2),
 };
 #undef CP_VARIANT
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
