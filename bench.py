@@ -495,9 +495,12 @@ def run_ours(args):
         threads = host_threads()
         rate, n_pts, dt = oracle_direct_rate(wd, args.cpu_seconds, threads)
         crate, c_pts, cdt = oracle_cutoff_rate(wc, args.cpu_seconds / 2, threads)
+        srate, s_pts, sdt = oracle_direct_rate(wd, args.cpu_seconds / 4, 1)
         cpu = {"value": rate, "unit": "pair evals/s", "cores": threads, "kind": "oracle",
                "sample": f"fp64 direct sum at {n_pts} seeded grid points of the {tuple(wd.shape)} grid x "
                          f"{wd.n_atoms} atoms ({dt:.1f} s)",
+               "single_core": {"value": srate, "unit": "pair evals/s", "cores": 1,
+                               "sample": f"the same sum at {s_pts} points on one thread ({sdt:.1f} s)"},
                "cutoff": {"value": crate, "unit": "grid points/s",
                           "sample": f"fp64 binned cutoff sum at {c_pts} seeded points ({cdt:.1f} s)"}}
 

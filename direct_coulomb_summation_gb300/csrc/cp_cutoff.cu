@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(256) bin_sort_pack_kernel(const __grid_constan
 
 constexpr int kBrickConsumerWarps = 4;
 constexpr int kBrickThreads = 32 * (kBrickConsumerWarps + 1);  // + 1 producer warp
-constexpr int kBrickStages = 8;
+constexpr int kBrickStages = 12;
 
 struct BrickParams {
     int nx, ny, nz;
@@ -255,13 +255,6 @@ struct BrickParams {
     unsigned long long *counts;  // pair-counting variant only: [3] see cp_cutoff_pair_counts
     int n_runs;
     int runs[kMaxRuns];  // packed int8 (dy, dz, dx_lo, dx_hi)
-};
-
-// One listed atom with each component duplicated and the coordinates
-// negated: (-x,-x), (-y,-y), (-z,-z), (q,q), so that point - atom is one
-// f32x2 add.
-struct __align__(16) AtomPair {
-    float2 x, y, z, q;
 };
 
 __device__ __forceinline__ int brick_home_dev(int brick, int m, double h, double b) {
@@ -286,7 +279,7 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
     __shared__ __align__(128) float4 ring[kBrickStages][kStageAtoms];
     // list b (atoms that can reach sub-box b) in segments, one per writing
     // warp, so that list order never depends on timing
-    __shared__ __align__(16) AtomPair wlist[kBrickConsumerWarps][kBrickConsumerWarps][kWarpSlots];
+    __shared__ __align__(16) float4 wlist[kBrickConsumerWarps][kBrickConsumerWarps][kWarpSlots];
     __shared__ int wcount[kBrickConsumerWarps][kBrickConsumerWarps];
     __shared__ volatile int abort_flag;
     __shared__ uint64_t full[kBrickStages], empty[kBrickStages];
@@ -429,11 +422,11 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
     const int yy = (warp & 1) * 4 + ((lane >> 1) & 3);
     const int zz = (warp >> 1) * 4 + (lane >> 3);
     const int i0 = kBrick * bx + xq, j = kBrick * by + yy, k = kBrick * bz + zz;
-    const float2 X01 = make_float2(fmaf((float)(i0 + 0), p.h, p.ox), fmaf((float)(i0 + 1), p.h, p.ox));
-    const float2 X23 = make_float2(fmaf((float)(i0 + 2), p.h, p.ox), fmaf((float)(i0 + 3), p.h, p.ox));
+    float x[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) x[c] = fmaf((float)(i0 + c), p.h, p.ox);
     const float y = fmaf((float)j, p.h, p.oy);
     const float z = fmaf((float)k, p.h, p.oz);
-    const float2 Y2 = make_float2(y, y), Z2 = make_float2(z, z);
     const float2 NG0 = make_float2(-p.gc0, -p.gc0), NG1 = make_float2(-p.gc1, -p.gc1);
     const float2 NG2 = make_float2(-p.gc2, -p.gc2);
     // the four sub-boxes share their x extent; two y and two z extents
@@ -454,7 +447,7 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
         if (n >= 0) {
             // (1) this warp's quarter of the stage against all four sub-boxes;
             // an atom that can reach sub-box b is appended to segment `warp`
-            // of list b (each component stored twice, coordinates negated)
+            // of list b
             const int i = kWarpSlots * warp + lane;
             const bool valid = i < n;
             const float4 a = valid ? ring[s][i] : make_float4(kPadCoord, kPadCoord, kPadCoord, 0.f);
@@ -465,14 +458,12 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
             const float ez0 = fmaxf(fmaxf(loz0 - a.z, a.z - hiz0), 0.0f);
             const float ez1 = fmaxf(fmaxf(loz1 - a.z, a.z - hiz1), 0.0f);
             const float e2y0 = fmaf(ey0, ey0, ex * ex), e2y1 = fmaf(ey1, ey1, ex * ex);
-            const AtomPair e = AtomPair{make_float2(-a.x, -a.x), make_float2(-a.y, -a.y), make_float2(-a.z, -a.z),
-                                        make_float2(a.w, a.w)};
 #pragma unroll
             for (int b = 0; b < kBrickConsumerWarps; ++b) {
                 const float ez = (b >> 1) ? ez1 : ez0;
                 const bool near = fmaf(ez, ez, (b & 1) ? e2y1 : e2y0) < p.cull2;
                 const unsigned m = __ballot_sync(0xffffffffu, near);
-                if (near) wlist[b][warp][__popc(m & below)] = e;
+                if (near) wlist[b][warp][__popc(m & below)] = a;
                 if (lane == 0) wcount[b][warp] = __popc(m);
             }
             __syncwarp();
@@ -486,15 +477,17 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
         for (int g = 0; g < kBrickConsumerWarps; ++g) {
             const int cnt = wcount[warp][g];
             if (COUNT) n_near += (unsigned)cnt;
-            const AtomPair *list = &wlist[warp][g][0];
+            const float4 *list = &wlist[warp][g][0];
 #pragma unroll 2
             for (int t = 0; t < cnt; ++t) {
-                const AtomPair a = list[t];  // broadcast
-                const float2 dy = __fadd2_rn(Y2, a.y);
-                const float2 dz = __fadd2_rn(Z2, a.z);
-                const float2 dyz2 = __ffma2_rn(dy, dy, __fmul2_rn(dz, dz));
-                const float2 dx01 = __fadd2_rn(X01, a.x);
-                const float2 dx23 = __fadd2_rn(X23, a.x);
+                const float4 a = list[t];  // broadcast
+                // differences as scalars (dy^2 + dz^2 is the same for the
+                // lane's 4 points), written into the f32x2 operand pairs
+                const float dy = y - a.y, dz = z - a.z;
+                const float d = fmaf(dy, dy, dz * dz);
+                const float2 dyz2 = make_float2(d, d);
+                const float2 dx01 = make_float2(x[0] - a.x, x[1] - a.x);
+                const float2 dx23 = make_float2(x[2] - a.x, x[3] - a.x);
                 const float2 r01 = __ffma2_rn(dx01, dx01, dyz2);
                 const float2 r23 = __ffma2_rn(dx23, dx23, dyz2);
                 // e = rsqrt(r^2) - g(r^2), with -g by Horner on the negated coefficients
@@ -502,10 +495,10 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
                 const float2 rs23 = make_float2(sfu_rsqrt(r23.x), sfu_rsqrt(r23.y));
                 const float2 e01 = __fadd2_rn(rs01, __ffma2_rn(__ffma2_rn(r01, NG2, NG1), r01, NG0));
                 const float2 e23 = __fadd2_rn(rs23, __ffma2_rn(__ffma2_rn(r23, NG2, NG1), r23, NG0));
-                if (r01.x < p.c2) part[0] = fmaf(a.q.x, e01.x, part[0]);
-                if (r01.y < p.c2) part[1] = fmaf(a.q.x, e01.y, part[1]);
-                if (r23.x < p.c2) part[2] = fmaf(a.q.x, e23.x, part[2]);
-                if (r23.y < p.c2) part[3] = fmaf(a.q.x, e23.y, part[3]);
+                if (r01.x < p.c2) part[0] = fmaf(a.w, e01.x, part[0]);
+                if (r01.y < p.c2) part[1] = fmaf(a.w, e01.y, part[1]);
+                if (r23.x < p.c2) part[2] = fmaf(a.w, e23.x, part[2]);
+                if (r23.y < p.c2) part[3] = fmaf(a.w, e23.y, part[3]);
                 if (COUNT) {
                     const float r2c[4] = {r01.x, r01.y, r23.x, r23.y};
 #pragma unroll
