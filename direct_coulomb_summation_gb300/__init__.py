@@ -7,6 +7,7 @@ every step of the computation runs in the library's CUDA kernels.
     import direct_coulomb_summation_gb300 as cp
     V = cp.direct(atoms, (nx, ny, nz), origin, h)                 # direct sum
     V = cp.cutoff(atoms, (nx, ny, nz), origin, h, 12.0, 4.0)      # cutoff sum
+    V = cp.msm_map(atoms, (nx, ny, nz), origin, h, 12.0, 4.0, 2.0) # cutoff + multilevel long range
 
 ``atoms`` is an (n, 4) float32 array of (x, y, z, q).  A CUDA tensor gives a
 CUDA result on the current stream (asynchronous); a CPU tensor or numpy
@@ -22,7 +23,7 @@ import numpy as np
 import torch
 
 from . import _lib
-from ._lib import cp_vec3
+from ._lib import cp_msm_layout, cp_vec3
 
 __all__ = [
     "CpError",
@@ -46,6 +47,11 @@ __all__ = [
     "version",
     "library",
     "DIRECT_VARIANTS",
+    "atom_bounds",
+    "msm_layout",
+    "msm_workspace_bytes",
+    "msm_longrange",
+    "msm_map",
 ]
 
 # index -> (PY, PZ, EMU): per-thread patch of 4 x-points times PY rows times PZ
@@ -228,6 +234,9 @@ def cutoff(atoms, shape, origin, h, cutoff, bin_size, capacity: int = 16, worksp
     return _finish_host(V, host_out) if on_host else V
 
 
+_cutoff_sum = cutoff  # msm_map's `cutoff` argument shadows the function
+
+
 def bin_atoms(atoms, shape, origin, h, cutoff, bin_size, capacity: int = 16, workspace=None, stream=None):
     """Runs only the binning stage; returns tensors viewing the workspace:
     count, start, csr_index, csr_atoms, padded (nbins, K, 4), plus the layout."""
@@ -332,3 +341,76 @@ def probe_pipe_rate(kind: str, warps: int = 32, iters: int = 4096, stream=None):
                                       _stream(stream))
     _check(rc, "cp_probe_pipe_rate")
     return float(r.value), float(ms.value)
+
+
+# ---------------------------------------------------------------------------
+# multilevel summation: long-range part
+
+
+def atom_bounds(atoms, stream=None):
+    """The atoms' bounding box ((min x, y, z), (max x, y, z)), computed by the
+    library's reduction kernel and read back (synchronises the stream)."""
+    lib = library()
+    dev_atoms, _ = _as_device_atoms(atoms)
+    n = int(dev_atoms.shape[0])
+    out = torch.empty(6, dtype=torch.float32, device=dev_atoms.device)
+    _check(lib.cp_atom_bounds(dev_atoms.data_ptr(), n, out.data_ptr(), _stream(stream)), "cp_atom_bounds")
+    b = out.cpu().numpy()
+    return tuple(float(v) for v in b[:3]), tuple(float(v) for v in b[3:])
+
+
+def _domain(domain, dev_atoms, stream):
+    if domain is not None:
+        return domain
+    if dev_atoms.shape[0] == 0:
+        return (0.0, 0.0, 0.0), (0.0, 0.0, 0.0)
+    return atom_bounds(dev_atoms, stream)
+
+
+def msm_layout(n_atoms, shape, origin, h, cutoff, lattice_h, domain) -> cp_msm_layout:
+    """Lattice levels, stencil and workspace layout (host-only)."""
+    L = cp_msm_layout()
+    lo, hi = domain
+    rc = library().cp_msm_layout_of(int(n_atoms), *_grid(shape, origin, h), _vec3(lo), _vec3(hi),
+                                    float(np.float32(cutoff)), float(np.float32(lattice_h)), ctypes.byref(L))
+    _check(rc, "cp_msm_layout_of")
+    return L
+
+
+def msm_workspace_bytes(n_atoms, shape, origin, h, cutoff, lattice_h, domain) -> int:
+    return int(msm_layout(n_atoms, shape, origin, h, cutoff, lattice_h, domain).total_bytes)
+
+
+def msm_longrange(atoms, shape, origin, h, cutoff, lattice_h, domain=None, accumulate: bool = False,
+                  workspace=None, out=None, stream=None, host_out=None):
+    """Multilevel approximation of V_long = sum_a q_a g_c(r) (the smooth part
+    of 1/r that the cutoff sum leaves out); returns V as (nz, ny, nx).
+
+    ``domain``: ((lo x, y, z), (hi x, y, z)) containing every atom; if None,
+    the atoms' bounding box from ``atom_bounds``.  ``accumulate`` adds into
+    ``out`` instead of overwriting it."""
+    lib = library()
+    dev_atoms, on_host = _as_device_atoms(atoms)
+    n = int(dev_atoms.shape[0])
+    lo, hi = _domain(domain, dev_atoms, stream)
+    need = msm_workspace_bytes(n, shape, origin, h, cutoff, lattice_h, (lo, hi))
+    ws = _workspace(workspace, need, dev_atoms.device)
+    if accumulate and out is None:
+        raise ValueError("accumulate=True needs out")
+    V = _out_tensor(out, shape, dev_atoms.device)
+    rc = lib.cp_msm_longrange(dev_atoms.data_ptr() if n else None, n, *_grid(shape, origin, h), _vec3(lo), _vec3(hi),
+                              float(np.float32(cutoff)), float(np.float32(lattice_h)), ws.data_ptr(),
+                              ws.numel() * ws.element_size(), V.data_ptr(), int(bool(accumulate)), _stream(stream))
+    _check(rc, "cp_msm_longrange")
+    return _finish_host(V, host_out) if on_host else V
+
+
+def msm_map(atoms, shape, origin, h, cutoff, bin_size, lattice_h, capacity: int = 0, domain=None, out=None,
+            stream=None, host_out=None):
+    """Multilevel approximation of the full direct sum: the cutoff map (short
+    range) plus the long-range part, both through the library."""
+    dev_atoms, on_host = _as_device_atoms(atoms)
+    V = _cutoff_sum(dev_atoms, shape, origin, h, cutoff, bin_size, capacity, out=out, stream=stream)
+    msm_longrange(dev_atoms, shape, origin, h, cutoff, lattice_h, domain=domain, accumulate=True, out=V,
+                  stream=stream)
+    return _finish_host(V, host_out) if on_host else V

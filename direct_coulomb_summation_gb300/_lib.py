@@ -47,6 +47,29 @@ class cp_cutoff_stats_t(ctypes.Structure):
     ]
 
 
+MSM_MAX_LEVELS = 16
+
+
+class cp_msm_layout(ctypes.Structure):
+    _fields_ = [
+        ("levels", ctypes.c_int),
+        ("lo", (ctypes.c_int * 3) * MSM_MAX_LEVELS),
+        ("n", (ctypes.c_int * 3) * MSM_MAX_LEVELS),
+        ("split", ctypes.c_int * MSM_MAX_LEVELS),
+        ("radius", ctypes.c_int),
+        ("taps", ctypes.c_int),
+        ("cells", ctypes.c_int * 3),
+        ("lattice_origin", cp_vec3),
+        ("q_dims", (ctypes.c_int * 3) * MSM_MAX_LEVELS),
+        ("off_q", ctypes.c_size_t * MSM_MAX_LEVELS),
+        ("off_e", ctypes.c_size_t * MSM_MAX_LEVELS),
+        ("off_cells", ctypes.c_size_t),
+        ("off_stencil", ctypes.c_size_t),
+        ("off_partial", ctypes.c_size_t),
+        ("total_bytes", ctypes.c_size_t),
+    ]
+
+
 _I, _F, _P, _SZ = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 _GRID = [_I, _I, _I, cp_vec3, _F]  # nx, ny, nz, origin, h
 
@@ -73,6 +96,10 @@ SIGNATURES = {
     "cp_cutoff27_workspace_bytes": (_SZ, [_I, *_GRID, _F]),
     "cp_cutoff27": (_I, [_P, _I, *_GRID, _F, _P, _SZ, _P, _P]),
     "cp_probe_pipe_rate": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _P]),
+    "cp_msm_layout_of": (_I, [_I, *_GRID, cp_vec3, cp_vec3, _F, _F, ctypes.POINTER(cp_msm_layout)]),
+    "cp_msm_workspace_bytes": (_SZ, [_I, *_GRID, cp_vec3, cp_vec3, _F, _F]),
+    "cp_msm_longrange": (_I, [_P, _I, *_GRID, cp_vec3, cp_vec3, _F, _F, _P, _SZ, _P, _I, _P]),
+    "cp_atom_bounds": (_I, [_P, _I, _P, _P]),
 }
 
 

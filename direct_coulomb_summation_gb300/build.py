@@ -23,7 +23,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libcpmap.so")
 STAMP = os.path.join(BUILD, "libcpmap.stamp")
 
-SOURCES = ["cp_host.cu", "cp_direct.cu", "cp_cutoff.cu", "cp_probe.cu", "cp_variants.cu"]
+SOURCES = ["cp_host.cu", "cp_direct.cu", "cp_cutoff.cu", "cp_msm.cu", "cp_probe.cu", "cp_variants.cu"]
 HEADERS = ["cp_device.cuh", "cp_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -546,6 +546,53 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
 
 namespace {
 
+// Kernel arguments of the binning kernels for the sections of `L` at `ws`.
+BinParams bin_params(const float4 *atoms, int n_atoms, const BinGeom &bg, const cp_cutoff_layout &L, void *workspace) {
+    char *ws = static_cast<char *>(workspace);
+    BinParams b;
+    b.atoms = atoms;
+    b.n = n_atoms;
+    for (int d = 0; d < 3; ++d) {
+        b.nb[d] = bg.nb[d];
+        b.bo[d] = bg.bo[d];
+    }
+    b.b = bg.b;
+    b.nbins = (int)bg.nbins;
+    b.K = L.capacity;
+    b.count = reinterpret_cast<int *>(ws + L.off_count);
+    b.start = reinterpret_cast<int *>(ws + L.off_start);
+    b.csr_index = reinterpret_cast<int *>(ws + L.off_csr_index);
+    b.csr_atoms = reinterpret_cast<float4 *>(ws + L.off_csr_atoms);
+    b.padded = reinterpret_cast<float4 *>(ws + L.off_padded);
+    b.stats = reinterpret_cast<int *>(ws + L.off_stats);
+    const size_t n = (size_t)(n_atoms > 0 ? n_atoms : 0);
+    const size_t nblk = ((size_t)bg.nbins + kScanBlock - 1) / kScanBlock;
+    size_t off = L.off_scratch;
+    b.bin_rank = reinterpret_cast<int2 *>(ws + off);
+    off += (8 * n + 255) & ~(size_t)255;
+    b.block_sums = reinterpret_cast<int *>(ws + off);
+    off += (4 * nblk + 255) & ~(size_t)255;
+    b.block_prefix = reinterpret_cast<int *>(ws + off);
+    return b;
+}
+
+int launch_binning_params(const BinParams &b, cudaStream_t stream) {
+    const int nblk = (int)(((long long)b.nbins + kScanBlock - 1) / kScanBlock);
+    DeviceInfo dev;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    const int clear_blocks = (int)std::min<long long>((b.nbins + 255) / 256, 8LL * dev.sm_count);
+    bin_clear_kernel<<<std::max(clear_blocks, 1), 256, 0, stream>>>(b);
+    if (b.n > 0) bin_count_kernel<<<(b.n + 255) / 256, 256, 0, stream>>>(b);
+    bin_scan_local_kernel<<<nblk, 256, 0, stream>>>(b);
+    bin_scan_blocks_kernel<<<1, 1024, 0, stream>>>(b, nblk);
+    if (b.n > 0) bin_scatter_kernel<<<(b.n + 255) / 256, 256, 0, stream>>>(b);
+    bin_sort_pack_kernel<<<(b.nbins + 7) / 8, 256, 0, stream>>>(b);
+    if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
+    note_launches(b.n > 0 ? 6 : 4);
+    return CP_OK;
+}
+
 struct Prepared {
     Grid g;
     BinGeom bg;
@@ -568,51 +615,11 @@ int prepare(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 ori
     if (rc) return rc;
     if (workspace_bytes < out->L.total_bytes) return CP_ERR_WORKSPACE_TOO_SMALL;
     if ((long long)out->bg.nbins * capacity > INT_MAX) return CP_ERR_TOO_LARGE;
-    char *ws = static_cast<char *>(workspace);
-    BinParams &b = out->bp;
-    b.atoms = reinterpret_cast<const float4 *>(atoms);
-    b.n = n_atoms;
-    for (int d = 0; d < 3; ++d) {
-        b.nb[d] = out->bg.nb[d];
-        b.bo[d] = out->bg.bo[d];
-    }
-    b.b = bin_size;
-    b.nbins = (int)out->bg.nbins;
-    b.K = capacity;
-    b.count = reinterpret_cast<int *>(ws + out->L.off_count);
-    b.start = reinterpret_cast<int *>(ws + out->L.off_start);
-    b.csr_index = reinterpret_cast<int *>(ws + out->L.off_csr_index);
-    b.csr_atoms = reinterpret_cast<float4 *>(ws + out->L.off_csr_atoms);
-    b.padded = reinterpret_cast<float4 *>(ws + out->L.off_padded);
-    b.stats = reinterpret_cast<int *>(ws + out->L.off_stats);
-    const size_t n = (size_t)n_atoms;
-    const size_t nblk = ((size_t)out->bg.nbins + kScanBlock - 1) / kScanBlock;
-    size_t off = out->L.off_scratch;
-    b.bin_rank = reinterpret_cast<int2 *>(ws + off);
-    off += (8 * n + 255) & ~(size_t)255;
-    b.block_sums = reinterpret_cast<int *>(ws + off);
-    off += (4 * nblk + 255) & ~(size_t)255;
-    b.block_prefix = reinterpret_cast<int *>(ws + off);
+    out->bp = bin_params(reinterpret_cast<const float4 *>(atoms), n_atoms, out->bg, out->L, workspace);
     return CP_OK;
 }
 
-int launch_binning(const Prepared &P, cudaStream_t stream) {
-    const BinParams &b = P.bp;
-    const int nblk = (int)(((long long)b.nbins + kScanBlock - 1) / kScanBlock);
-    DeviceInfo dev;
-    int rc = device_info(&dev);
-    if (rc) return rc;
-    const int clear_blocks = (int)std::min<long long>((b.nbins + 255) / 256, 8LL * dev.sm_count);
-    bin_clear_kernel<<<std::max(clear_blocks, 1), 256, 0, stream>>>(b);
-    if (b.n > 0) bin_count_kernel<<<(b.n + 255) / 256, 256, 0, stream>>>(b);
-    bin_scan_local_kernel<<<nblk, 256, 0, stream>>>(b);
-    bin_scan_blocks_kernel<<<1, 1024, 0, stream>>>(b, nblk);
-    if (b.n > 0) bin_scatter_kernel<<<(b.n + 255) / 256, 256, 0, stream>>>(b);
-    bin_sort_pack_kernel<<<(b.nbins + 7) / 8, 256, 0, stream>>>(b);
-    if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
-    note_launches(b.n > 0 ? 6 : 4);
-    return CP_OK;
-}
+int launch_binning(const Prepared &P, cudaStream_t stream) { return launch_binning_params(P.bp, stream); }
 
 template <int K>
 int launch_bricks_k(const Prepared &P, const OffsetList &L, float *V, cudaStream_t stream,
@@ -677,6 +684,12 @@ int launch_bricks(const Prepared &P, const OffsetList &L, float *V, cudaStream_t
 }
 
 }  // namespace
+
+int sort_atoms_into_cells(const float4 *atoms, int n_atoms, const BinGeom &bg, const cp_cutoff_layout &L,
+                          void *workspace, cudaStream_t stream) {
+    if (L.capacity != 0 || L.nbins != bg.nbins) return CP_ERR_INVALID_ARGUMENT;
+    return launch_binning_params(bin_params(atoms, n_atoms, bg, L, workspace), stream);
+}
 
 }  // namespace cpmap
 

@@ -53,6 +53,14 @@ int make_offset_list(const Grid &g, const BinGeom &bg, OffsetList *out);
 int make_layout(int n_atoms, const BinGeom &bg, int capacity, cp_cutoff_layout *out);
 
 // Per-device facts (cached after the first query on each device).
+// Deterministic counting sort of atoms into the cells of `bg` (no fixed
+// slots: L from make_layout(n, bg, 0, &L)), leaving count, start, the
+// cell-sorted atoms and indices (ascending input index within a cell) and
+// the stats in the sections of `workspace`.  Atoms outside the cell grid
+// are dropped and counted in stats[1].
+int sort_atoms_into_cells(const float4 *atoms, int n_atoms, const BinGeom &bg, const cp_cutoff_layout &L,
+                          void *workspace, cudaStream_t stream);
+
 struct DeviceInfo {
     int device;
     int sm_count;

@@ -1,0 +1,768 @@
+// cp_msm.cu -- long-range part of a multilevel summation on sm_103a.
+//
+// The Input Binning lecture's slide "Large Bin Cut-off Kernel Code" (24)
+// names its cutoff kernel mgpot_shortrng_energy: the switched sum that
+// cp_cutoff computes is the short-range part of a multilevel summation of
+// 1/r.  The smooth remainder V_long(x) = sum_a q_a g_c(|x - r_a|) (g_c = the
+// switching polynomial inside c, 1/r beyond) is approximated here on nested
+// lattices (R. D. Skeel, I. Tezcan, D. J. Hardy, "Multiple grid methods for
+// classical molecular dynamics", J. Comput. Chem. 23 (2002); D. J. Hardy,
+// J. E. Stone, K. Schulten, "Multilevel summation of electrostatic
+// potentials using graphics processing units", Parallel Computing 35
+// (2009)).  The pages do not describe this part.
+//
+// GPU mapping:
+//   * anterpolation as a gather: the atoms are counting-sorted into the
+//     level-0 lattice cells (the cutoff path's binning kernels), then every
+//     node sums the atoms of the 4x4x4 cells its basis function covers, in
+//     a fixed order -- no atomics, deterministic;
+//   * charge lattices are stored with R zero nodes of padding on every side
+//     (z rounded up to whole 8-node columns), so the lattice-cutoff stencil
+//     reads them without bounds checks;
+//   * lattice cutoff: a thread owns 8 nodes stacked in z and walks the
+//     stencil column by column (fixed dy, dx; dz innermost), so each tap is
+//     one coalesced load of the next node of a sliding 8-node window, one
+//     uniform weight load and 8 FMAs.  All levels below the top run in one
+//     launch; the stencil columns of a tile are split over S CTAs whose
+//     partial sums are added in a fixed order afterwards;
+//   * top level: one warp per node, lanes split the other nodes, kernel
+//     values from a table indexed by |d|^2, a fixed-order warp reduction;
+//   * prolongation fused with that partial-sum reduction, level by level
+//     from the top down;
+//   * interpolation: a thread owns 4 consecutive x points of one row (a
+//     float4 of V); it sums the lattice columns its points share once.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstring>
+
+#include "cp_device.cuh"
+#include "cp_internal.h"
+
+namespace cpmap {
+
+constexpr int kMsmMaxLevels = CP_MSM_MAX_LEVELS;
+constexpr int kMsmMaxRadius = CP_MSM_MAX_RADIUS;
+constexpr int kMsmSide = 2 * kMsmMaxRadius + 1;
+constexpr int kMsmTopNodes = 12;                              // top level: at most 12 nodes per axis
+constexpr int kMsmTopTable = 3 * (kMsmTopNodes - 1) * (kMsmTopNodes - 1) + 1;  // |d|^2 values
+constexpr int kMsmZ = 8;                                      // nodes a lattice-cutoff thread stacks in z
+constexpr long long kMsmTargetThreads = 1LL << 17;            // lattice-cutoff threads worth splitting for
+constexpr int kMsmMaxSplit = 64;
+constexpr int kMsmThreads = 128;
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// device helpers
+
+// The C1 cubic interpolating basis function, support |t| < 2.
+__device__ __forceinline__ float msm_phi(float t) {
+    const float a = fabsf(t);
+    if (a <= 1.0f) return (1.0f - a) * (1.0f + a - 1.5f * a * a);
+    if (a <= 2.0f) {
+        const float b = 2.0f - a;
+        return -0.5f * (a - 1.0f) * b * b;
+    }
+    return 0.0f;
+}
+
+// g_c(r) = gamma(r/c)/c in fp64 with explicit roundings (no contraction).
+__device__ double msm_g64(double r, double c) {
+    const double s = __ddiv_rn(r, c);
+    if (s < 1.0) {
+        const double s2 = __dmul_rn(s, s);
+        const double p = __dadd_rn(__dadd_rn(1.875, __dmul_rn(-1.25, s2)), __dmul_rn(0.375, __dmul_rn(s2, s2)));
+        return __ddiv_rn(p, c);
+    }
+    return __ddiv_rn(1.0, r);
+}
+
+// Lattice coordinate of x relative to the lattice origin, in units of h0:
+// the same fp32 expression the cell sort uses for the cell index.
+__device__ __forceinline__ float msm_t(float x, float o, float h0) { return __fdiv_rn(__fsub_rn(x, o), h0); }
+
+struct MsmLevelDev {
+    int lo[3], n[3];
+    int qd[3];              // padded charge lattice dims (x, y, z)
+    float *q;               // padded charges
+    float *e;               // potentials [n z][n y][n x]
+    float *part;            // partial sums [split][n z][n y][n x]
+    int split;
+    long long cols;         // lattice-cutoff threads of this level (x * y * z-stacks)
+    long long cta_begin;    // first lattice-cutoff CTA of this level
+    float scale;            // 2^-l
+};
+
+struct MsmParams {
+    int levels;  // L + 1
+    MsmLevelDev lv[kMsmMaxLevels];
+    int R;
+    float *W;      // [2R+1]^3 stencil, symmetric in its three indices
+    float *gtop;   // top-level kernel by |d|^2
+    int cells[3];
+    float o[3];
+    float h0;
+    const int *cell_start;
+    const float4 *cell_atoms;
+    const int *cell_stats;
+    unsigned int *status;
+    double h0_64, a64, lim2;
+    int8_t hw[kMsmSide * kMsmSide];  // stencil column (dy, dx) half height in dz, -1 if empty
+};
+
+// ---------------------------------------------------------------------------
+// kernels
+
+// W(d) = g_c(|d| h0) - g_2c(|d| h0) for |d|^2 < (2c/h0)^2, else 0; and the
+// top-level table 2^-L g_c(sqrt(s) h0) for s = 0 .. 3*11^2.
+__global__ void msm_stencil_kernel(const __grid_constant__ MsmParams p) {
+    const int side = 2 * p.R + 1;
+    const int n = side * side * side;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n + kMsmTopTable; idx += stride) {
+        if (idx < n) {
+            const int dx = (int)(idx % side) - p.R;
+            const int dy = (int)((idx / side) % side) - p.R;
+            const int dz = (int)(idx / ((long long)side * side)) - p.R;
+            const int s2 = dx * dx + dy * dy + dz * dz;
+            float w = 0.0f;
+            if ((double)s2 < p.lim2) {
+                const double r = __dmul_rn(__dsqrt_rn((double)s2), p.h0_64);
+                w = (float)__dsub_rn(msm_g64(r, p.a64), msm_g64(r, 2.0 * p.a64));
+            }
+            p.W[idx] = w;
+        } else {
+            const int s2 = (int)(idx - n);
+            const int L = p.levels - 1;
+            const double r = __dmul_rn(__dsqrt_rn((double)s2), p.h0_64);
+            p.gtop[s2] = (float)ldexp(msm_g64(r, p.a64), -L);
+        }
+    }
+}
+
+// q0 at every padded level-0 entry: zero in the padding, else the sum over
+// the atoms of the cells i-2 .. i+1 (per axis) of q Phi(t - i).
+__global__ void __launch_bounds__(kMsmThreads) msm_anterp_kernel(const __grid_constant__ MsmParams p) {
+    const MsmLevelDev &L0 = p.lv[0];
+    const long long total = (long long)L0.qd[0] * L0.qd[1] * L0.qd[2];
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int px = (int)(idx % L0.qd[0]);
+    const int py = (int)((idx / L0.qd[0]) % L0.qd[1]);
+    const int pz = (int)(idx / ((long long)L0.qd[0] * L0.qd[1]));
+    const int ax = px - p.R, ay = py - p.R, az = pz - p.R;  // array index within the level
+    float acc = 0.0f;
+    if (ax >= 0 && ax < L0.n[0] && ay >= 0 && ay < L0.n[1] && az >= 0 && az < L0.n[2]) {
+        const int i = ax + L0.lo[0], j = ay + L0.lo[1], k = az + L0.lo[2];  // node index
+        const int cx0 = max(i - 2, 0), cx1 = min(i + 1, p.cells[0] - 1);
+        const int cy0 = max(j - 2, 0), cy1 = min(j + 1, p.cells[1] - 1);
+        const int cz0 = max(k - 2, 0), cz1 = min(k + 1, p.cells[2] - 1);
+        if (cx0 <= cx1) {
+            for (int cz = cz0; cz <= cz1; ++cz)
+                for (int cy = cy0; cy <= cy1; ++cy) {
+                    const long long row = ((long long)cz * p.cells[1] + cy) * p.cells[0];
+                    const int b = p.cell_start[row + cx0], e = p.cell_start[row + cx1 + 1];
+                    for (int t = b; t < e; ++t) {
+                        const float4 a = p.cell_atoms[t];
+                        const float wx = msm_phi(msm_t(a.x, p.o[0], p.h0) - (float)i);
+                        const float wy = msm_phi(msm_t(a.y, p.o[1], p.h0) - (float)j);
+                        const float wz = msm_phi(msm_t(a.z, p.o[2], p.h0) - (float)k);
+                        acc = fmaf(a.w, wx * wy * wz, acc);
+                    }
+                }
+        }
+    }
+    L0.q[idx] = acc;
+}
+
+// Restriction weights phi(k/2) for fine offsets k = -3 .. 3 (k = +-2 weigh 0).
+__device__ __forceinline__ float msm_rw(int k) {
+    switch (k) {
+        case 0: return 1.0f;
+        case 1:
+        case -1: return 0.5625f;
+        case 3:
+        case -3: return -0.0625f;
+        default: return 0.0f;
+    }
+}
+
+// q(l+1) at every padded entry: zero in the padding, else
+// sum_k w(kx) w(ky) w(kz) q(l)[2J + k] over the fine nodes that exist.
+__global__ void __launch_bounds__(kMsmThreads) msm_restrict_kernel(const __grid_constant__ MsmParams p, int l) {
+    const MsmLevelDev &F = p.lv[l];
+    const MsmLevelDev &C = p.lv[l + 1];
+    const long long total = (long long)C.qd[0] * C.qd[1] * C.qd[2];
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int px = (int)(idx % C.qd[0]);
+    const int py = (int)((idx / C.qd[0]) % C.qd[1]);
+    const int pz = (int)(idx / ((long long)C.qd[0] * C.qd[1]));
+    const int ax = px - p.R, ay = py - p.R, az = pz - p.R;
+    float acc = 0.0f;
+    if (ax >= 0 && ax < C.n[0] && ay >= 0 && ay < C.n[1] && az >= 0 && az < C.n[2]) {
+        const int J[3] = {ax + C.lo[0], ay + C.lo[1], az + C.lo[2]};
+        for (int kz = -3; kz <= 3; ++kz) {
+            const float wz = msm_rw(kz);
+            const int fz = 2 * J[2] + kz - F.lo[2];
+            if (wz == 0.0f || fz < 0 || fz >= F.n[2]) continue;
+            for (int ky = -3; ky <= 3; ++ky) {
+                const float wy = msm_rw(ky);
+                const int fy = 2 * J[1] + ky - F.lo[1];
+                if (wy == 0.0f || fy < 0 || fy >= F.n[1]) continue;
+                const float *row = F.q + ((long long)(fz + p.R) * F.qd[1] + (fy + p.R)) * F.qd[0] + p.R;
+                float s = 0.0f;
+                for (int kx = -3; kx <= 3; ++kx) {
+                    const float wx = msm_rw(kx);
+                    const int fx = 2 * J[0] + kx - F.lo[0];
+                    if (wx == 0.0f || fx < 0 || fx >= F.n[0]) continue;
+                    s = fmaf(wx, row[fx], s);
+                }
+                acc = fmaf(wz * wy, s, acc);
+            }
+        }
+    }
+    C.q[idx] = acc;
+}
+
+// Lattice cutoff of every level below the top.  CTA -> (level, tile,
+// split); thread -> 8 nodes (x, y, z0 .. z0+7) of the level.  Split s of S
+// takes the stencil columns c = s, s + S, ...; a column (dy, dx) covers
+// dz = -hw .. hw.  The padded charge lattice makes every read in range.
+__global__ void __launch_bounds__(kMsmThreads) msm_conv_kernel(const __grid_constant__ MsmParams p) {
+    int l = 0;
+    while (l + 2 < p.levels && (long long)blockIdx.x >= p.lv[l + 1].cta_begin) ++l;
+    const MsmLevelDev &Lv = p.lv[l];
+    const long long local = (long long)blockIdx.x - Lv.cta_begin;
+    const int S = Lv.split;
+    const int s = (int)(local % S);
+    const long long col = (local / S) * kMsmThreads + threadIdx.x;
+    if (col >= Lv.cols) return;
+    const int x = (int)(col % Lv.n[0]);
+    const int y = (int)((col / Lv.n[0]) % Lv.n[1]);
+    const int z0 = (int)(col / ((long long)Lv.n[0] * Lv.n[1])) * kMsmZ;
+    const int R = p.R, side = 2 * R + 1;
+    const long long plane = (long long)Lv.qd[0] * Lv.qd[1];
+    const float *base = Lv.q + (long long)(z0 + R) * plane + (long long)(y + R) * Lv.qd[0] + (x + R);
+    float acc[kMsmZ];
+#pragma unroll
+    for (int t = 0; t < kMsmZ; ++t) acc[t] = 0.0f;
+    const int ncols = side * side;
+    for (int c = s; c < ncols; c += S) {
+        const int hw = p.hw[c];
+        if (hw < 0) continue;
+        const int dy = c / side - R, dx = c % side - R;
+        const float *q = base + (long long)dy * Lv.qd[0] + dx;
+        const float *w = p.W + (long long)c * side + R;  // W(dy, dx, dz) at w[dz]
+        float v[kMsmZ];
+#pragma unroll
+        for (int t = 0; t < kMsmZ - 1; ++t) v[t] = q[(long long)(t - hw) * plane];
+        for (int dz = -hw; dz <= hw; ++dz) {
+            v[kMsmZ - 1] = q[(long long)(dz + kMsmZ - 1) * plane];
+            const float wd = __ldg(w + dz);
+#pragma unroll
+            for (int t = 0; t < kMsmZ; ++t) acc[t] = fmaf(wd, v[t], acc[t]);
+#pragma unroll
+            for (int t = 0; t < kMsmZ - 1; ++t) v[t] = v[t + 1];
+        }
+    }
+    const long long nodes = (long long)Lv.n[0] * Lv.n[1] * Lv.n[2];
+    float *out = Lv.part + (long long)s * nodes + (long long)y * Lv.n[0] + x;
+#pragma unroll
+    for (int t = 0; t < kMsmZ; ++t)
+        if (z0 + t < Lv.n[2]) out[(long long)(z0 + t) * Lv.n[0] * Lv.n[1]] = acc[t];
+}
+
+// Top level: e_i = sum_j gtop[|i - j|^2] q_j over all top nodes; one warp
+// per node, lanes take every 32nd node, fixed-order reduction.
+__global__ void __launch_bounds__(kMsmThreads) msm_top_kernel(const __grid_constant__ MsmParams p) {
+    const MsmLevelDev &T = p.lv[p.levels - 1];
+    const int nodes = T.n[0] * T.n[1] * T.n[2];
+    const int node = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (node >= nodes) return;
+    const int ix = node % T.n[0], iy = (node / T.n[0]) % T.n[1], iz = node / (T.n[0] * T.n[1]);
+    float acc = 0.0f;
+    for (int j = lane; j < nodes; j += 32) {
+        const int jx = j % T.n[0], jy = (j / T.n[0]) % T.n[1], jz = j / (T.n[0] * T.n[1]);
+        const int dx = ix - jx, dy = iy - jy, dz = iz - jz;
+        const float q = T.q[((long long)(jz + p.R) * T.qd[1] + (jy + p.R)) * T.qd[0] + (jx + p.R)];
+        acc = fmaf(p.gtop[dx * dx + dy * dy + dz * dz], q, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, o);
+    if (lane == 0) T.e[node] = acc;
+}
+
+// Prolongation weight phi(i/2 - J) for fine index i and coarse index J.
+__device__ __forceinline__ int msm_prolong_taps(int i, int J0[4], float w[4]) {
+    if ((i & 1) == 0) {
+        J0[0] = i / 2;
+        w[0] = 1.0f;
+        return 1;
+    }
+    const int h = (i - 1) >> 1;  // floor(i/2) for odd i, also negative
+    J0[0] = h - 1;
+    w[0] = -0.0625f;
+    J0[1] = h;
+    w[1] = 0.5625f;
+    J0[2] = h + 1;
+    w[2] = 0.5625f;
+    J0[3] = h + 2;
+    w[3] = -0.0625f;
+    return 4;
+}
+
+// e(l) = 2^-l * (sum of the S partial sums, in split order) + the level-l+1
+// potentials interpolated to the level-l nodes.
+__global__ void __launch_bounds__(kMsmThreads) msm_reduce_prolong_kernel(const __grid_constant__ MsmParams p, int l) {
+    const MsmLevelDev &F = p.lv[l];
+    const MsmLevelDev &C = p.lv[l + 1];
+    const long long nodes = (long long)F.n[0] * F.n[1] * F.n[2];
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= nodes) return;
+    float s = 0.0f;
+    for (int k = 0; k < F.split; ++k) s += F.part[(long long)k * nodes + idx];
+    const int ax = (int)(idx % F.n[0]);
+    const int ay = (int)((idx / F.n[0]) % F.n[1]);
+    const int az = (int)(idx / ((long long)F.n[0] * F.n[1]));
+    int Jx[4], Jy[4], Jz[4];
+    float wx[4], wy[4], wz[4];
+    const int nx = msm_prolong_taps(ax + F.lo[0], Jx, wx);
+    const int ny = msm_prolong_taps(ay + F.lo[1], Jy, wy);
+    const int nz = msm_prolong_taps(az + F.lo[2], Jz, wz);
+    float pr = 0.0f;
+    for (int c = 0; c < nz; ++c) {
+        const int cz = Jz[c] - C.lo[2];
+        if (cz < 0 || cz >= C.n[2]) continue;
+        for (int b = 0; b < ny; ++b) {
+            const int cy = Jy[b] - C.lo[1];
+            if (cy < 0 || cy >= C.n[1]) continue;
+            const float *row = C.e + ((long long)cz * C.n[1] + cy) * C.n[0];
+            float r = 0.0f;
+            for (int a = 0; a < nx; ++a) {
+                const int cx = Jx[a] - C.lo[0];
+                if (cx >= 0 && cx < C.n[0]) r = fmaf(wx[a], row[cx], r);
+            }
+            pr = fmaf(wz[c] * wy[b], r, pr);
+        }
+    }
+    F.e[idx] = fmaf(F.scale, s, pr);
+}
+
+struct InterpParams {
+    int nx, ny, nz;
+    float ox, oy, oz, h;
+    long long quads;
+    int qx;
+    float *V;
+    int accumulate;
+};
+
+template <bool VEC>
+__global__ void __launch_bounds__(kMsmThreads) msm_interp_kernel(const __grid_constant__ MsmParams p,
+                                                                  const __grid_constant__ InterpParams g) {
+    const long long quad = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (quad == 0 && p.cell_stats[1] != 0) atomicOr(p.status, CP_DEVICE_ATOMS_OUTSIDE);
+    if (quad >= g.quads) return;
+    const int qx = (int)(quad % g.qx);
+    const int j = (int)((quad / g.qx) % g.ny);
+    const int k = (int)(quad / ((long long)g.qx * g.ny));
+    const int i0 = 4 * qx;
+    const MsmLevelDev &L0 = p.lv[0];
+    const float ty = msm_t(fmaf((float)j, g.h, g.oy), p.o[1], p.h0);
+    const float tz = msm_t(fmaf((float)k, g.h, g.oz), p.o[2], p.h0);
+    const int ky = (int)floorf(ty), kz = (int)floorf(tz);
+    float wy[4], wz[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        wy[b] = msm_phi(ty - (float)(ky - 1 + b));
+        wz[b] = msm_phi(tz - (float)(kz - 1 + b));
+    }
+    float tx[4];
+    int kx[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        tx[c] = msm_t(fmaf((float)min(i0 + c, g.nx - 1), g.h, g.ox), p.o[0], p.h0);
+        kx[c] = (int)floorf(tx[c]);
+    }
+    // node (i, j, k) of level 0 at e[(k - lo z) ...]
+    const float *e = L0.e;
+    const int n0 = L0.n[0], n1 = L0.n[1], n2 = L0.n[2];
+    auto column = [&](int ix) {  // sum over the 4x4 (y, z) nodes of lattice column ix
+        float s = 0.0f;
+        const int ax = ix - L0.lo[0];
+        if (ax < 0 || ax >= n0) return s;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int az = kz - 1 + c - L0.lo[2];
+            if (az < 0 || az >= n2) continue;
+            float r = 0.0f;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int ay = ky - 1 + b - L0.lo[1];
+                if (ay >= 0 && ay < n1) r = fmaf(wy[b], e[((long long)az * n1 + ay) * n0 + ax], r);
+            }
+            s = fmaf(wz[c], r, s);
+        }
+        return s;
+    };
+    float v[4];
+    const int kmin = kx[0], kmax = kx[3];
+    if (kmax - kmin <= 3) {
+        float cols[7];
+#pragma unroll
+        for (int m = 0; m < 7; ++m) cols[m] = (m <= kmax - kmin + 3) ? column(kmin - 1 + m) : 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float s = 0.0f;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int m = kx[c] - kmin + a;
+                float cv = 0.0f;
+#pragma unroll
+                for (int mm = 0; mm < 7; ++mm) cv = (mm == m) ? cols[mm] : cv;
+                s = fmaf(msm_phi(tx[c] - (float)(kx[c] - 1 + a)), cv, s);
+            }
+            v[c] = s;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float s = 0.0f;
+            for (int a = 0; a < 4; ++a) s = fmaf(msm_phi(tx[c] - (float)(kx[c] - 1 + a)), column(kx[c] - 1 + a), s);
+            v[c] = s;
+        }
+    }
+    float *row = g.V + ((long long)k * g.ny + j) * g.nx;
+    if (VEC) {
+        float4 *dst = reinterpret_cast<float4 *>(row + i0);
+        float4 out = make_float4(v[0], v[1], v[2], v[3]);
+        if (g.accumulate) {
+            const float4 old = *dst;
+            out.x += old.x;
+            out.y += old.y;
+            out.z += old.z;
+            out.w += old.w;
+        }
+        *dst = out;
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (i0 + c < g.nx) row[i0 + c] = g.accumulate ? row[i0 + c] + v[c] : v[c];
+    }
+}
+
+// Bounding box of the atoms, one CTA: per-thread min/max, then a tree
+// reduction in shared memory (min and max do not depend on the order).
+__global__ void __launch_bounds__(1024) atom_bounds_kernel(const float4 *atoms, int n, float *out) {
+    __shared__ float red[6][1024];
+    float lo[3] = {INFINITY, INFINITY, INFINITY}, hi[3] = {-INFINITY, -INFINITY, -INFINITY};
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const float4 a = atoms[i];
+        lo[0] = fminf(lo[0], a.x);
+        lo[1] = fminf(lo[1], a.y);
+        lo[2] = fminf(lo[2], a.z);
+        hi[0] = fmaxf(hi[0], a.x);
+        hi[1] = fmaxf(hi[1], a.y);
+        hi[2] = fmaxf(hi[2], a.z);
+    }
+    for (int d = 0; d < 3; ++d) {
+        red[d][threadIdx.x] = lo[d];
+        red[3 + d][threadIdx.x] = hi[d];
+    }
+    __syncthreads();
+    for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w)
+            for (int d = 0; d < 3; ++d) {
+                red[d][threadIdx.x] = fminf(red[d][threadIdx.x], red[d][threadIdx.x + w]);
+                red[3 + d][threadIdx.x] = fmaxf(red[3 + d][threadIdx.x], red[3 + d][threadIdx.x + w]);
+            }
+        __syncthreads();
+    }
+    if (threadIdx.x < 6) out[threadIdx.x] = red[threadIdx.x][0];
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct MsmGeom {
+    cp_msm_layout lay;
+    double o[3], h0, a, lim2;
+    BinGeom cells;
+    cp_cutoff_layout sortL;
+    size_t off_gtop;
+    size_t off_part[kMsmMaxLevels];
+    int8_t hw[kMsmSide * kMsmSide];
+};
+
+int make_msm_geometry(int n_atoms, const Grid &g, cp_vec3 dlo, cp_vec3 dhi, float cutoff, float lattice_h,
+                      MsmGeom *out) {
+    std::memset(out, 0, sizeof(*out));
+    const float dl[3] = {dlo.x, dlo.y, dlo.z}, dh[3] = {dhi.x, dhi.y, dhi.z};
+    for (int d = 0; d < 3; ++d)
+        if (!std::isfinite(dl[d]) || !std::isfinite(dh[d]) || dh[d] < dl[d]) return CP_ERR_INVALID_ARGUMENT;
+    if (n_atoms < 0 || !std::isfinite(cutoff) || !(cutoff > 0.0f) || !std::isfinite(lattice_h) ||
+        !(lattice_h > 0.0f))
+        return CP_ERR_INVALID_ARGUMENT;
+    const double h0 = lattice_h, a = cutoff;
+    const double ratio = 2.0 * a / h0;
+    if (!(ratio <= (double)kMsmMaxRadius)) return CP_ERR_TOO_LARGE;
+    const int R = std::max(1, (int)std::ceil(ratio));
+    const double go[3] = {g.ox, g.oy, g.oz};
+    const int gn[3] = {g.nx, g.ny, g.nz};
+    double hi[3];
+    long long ncells = 1;
+    cp_msm_layout &L = out->lay;
+    for (int d = 0; d < 3; ++d) {
+        const double lo = std::min((double)dl[d], go[d]);
+        hi[d] = std::max((double)dh[d], go[d] + (double)(gn[d] - 1) * (double)g.h);
+        out->o[d] = lo;
+        const double T = std::floor((hi[d] - lo) / h0);
+        if (!(T < 1.0e6)) return CP_ERR_TOO_LARGE;
+        L.cells[d] = (int)T + 2;
+        ncells *= L.cells[d];
+    }
+    if (ncells > (long long)kMaxScanBlocks * kScanBlock) return CP_ERR_TOO_LARGE;
+    L.lattice_origin = cp_vec3{(float)out->o[0], (float)out->o[1], (float)out->o[2]};
+    out->h0 = h0;
+    out->a = a;
+    out->lim2 = ratio * ratio;
+    L.radius = R;
+    // stencil columns and taps
+    const int side = 2 * R + 1;
+    int taps = 0, ncols = 0;
+    for (int c = 0; c < side * side; ++c) {
+        const int dy = c / side - R, dx = c % side - R;
+        int hwv = -1;
+        for (int dz = 0; dz <= R; ++dz)
+            if ((double)(dx * dx + dy * dy + dz * dz) < out->lim2) hwv = dz;
+        out->hw[c] = (int8_t)hwv;
+        if (hwv >= 0) {
+            taps += 2 * hwv + 1;
+            ++ncols;
+        }
+    }
+    L.taps = taps;
+    // levels
+    int lo[3] = {-1, -1, -1}, hiI[3] = {L.cells[0] + 1, L.cells[1] + 1, L.cells[2] + 1};
+    int levels = 0;
+    for (;;) {
+        if (levels == kMsmMaxLevels) return CP_ERR_TOO_LARGE;
+        int mx = 0;
+        for (int d = 0; d < 3; ++d) {
+            L.lo[levels][d] = lo[d];
+            L.n[levels][d] = hiI[d] - lo[d] + 1;
+            mx = std::max(mx, L.n[levels][d]);
+        }
+        ++levels;
+        if (mx <= kMsmTopNodes) break;
+        for (int d = 0; d < 3; ++d) {
+            lo[d] = (int)std::floor(lo[d] / 2.0) - 1;
+            hiI[d] = (int)std::ceil(hiI[d] / 2.0) + 1;
+        }
+    }
+    L.levels = levels;
+    // layout
+    size_t off = 0;
+    out->cells.nb[0] = L.cells[0];
+    out->cells.nb[1] = L.cells[1];
+    out->cells.nb[2] = L.cells[2];
+    for (int d = 0; d < 3; ++d) out->cells.bo[d] = (&L.lattice_origin.x)[d];
+    out->cells.nbins = ncells;
+    out->cells.b = lattice_h;
+    out->cells.c = cutoff;
+    out->cells.m = 0;
+    int rc = make_layout(n_atoms, out->cells, 0, &out->sortL);
+    if (rc) return rc;
+    L.off_cells = off;
+    off = align256(off + out->sortL.total_bytes);
+    L.off_stencil = off;
+    off = align256(off + 4 * (size_t)side * side * side);
+    out->off_gtop = off;
+    off = align256(off + 4 * (size_t)kMsmTopTable);
+    for (int l = 0; l < levels; ++l) {
+        const long long n0 = L.n[l][0], n1 = L.n[l][1], n2 = L.n[l][2];
+        L.q_dims[l][0] = (int)n0 + 2 * R;
+        L.q_dims[l][1] = (int)n1 + 2 * R;
+        L.q_dims[l][2] = (int)(kMsmZ * ((n2 + kMsmZ - 1) / kMsmZ)) + 2 * R;
+        const long long qn = (long long)L.q_dims[l][0] * L.q_dims[l][1] * L.q_dims[l][2];
+        if (qn > INT_MAX) return CP_ERR_TOO_LARGE;
+        L.off_q[l] = off;
+        off = align256(off + 4 * (size_t)qn);
+        L.off_e[l] = off;
+        off = align256(off + 4 * (size_t)(n0 * n1 * n2));
+    }
+    L.off_partial = off;
+    for (int l = 0; l + 1 < levels; ++l) {
+        const long long cols = (long long)L.n[l][0] * L.n[l][1] * ((L.n[l][2] + kMsmZ - 1) / kMsmZ);
+        const long long want = (kMsmTargetThreads + cols - 1) / cols;
+        L.split[l] = (int)std::max(1LL, std::min<long long>({want, (long long)kMsmMaxSplit, (long long)ncols}));
+        out->off_part[l] = off;
+        off = align256(off + 4 * (size_t)L.split[l] * (size_t)(L.n[l][0] * L.n[l][1] * L.n[l][2]));
+    }
+    L.total_bytes = off;
+    return CP_OK;
+}
+
+int prepare_msm(int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, cp_vec3 dlo, cp_vec3 dhi,
+                float cutoff, float lattice_h, Grid *g, MsmGeom *geo) {
+    int rc = check_grid(nx, ny, nz, origin, h, g);
+    if (rc) return rc;
+    return make_msm_geometry(n_atoms, *g, dlo, dhi, cutoff, lattice_h, geo);
+}
+
+}  // namespace
+
+}  // namespace cpmap
+
+using namespace cpmap;
+
+extern "C" {
+
+CP_API int cp_msm_layout_of(int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, cp_vec3 domain_lo,
+                            cp_vec3 domain_hi, float cutoff, float lattice_h, cp_msm_layout *out) {
+    if (!out) return CP_ERR_INVALID_ARGUMENT;
+    Grid g;
+    static thread_local MsmGeom geo;
+    const int rc = prepare_msm(n_atoms, nx, ny, nz, origin, h, domain_lo, domain_hi, cutoff, lattice_h, &g, &geo);
+    if (rc) return rc;
+    *out = geo.lay;
+    return CP_OK;
+}
+
+CP_API size_t cp_msm_workspace_bytes(int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                                     cp_vec3 domain_lo, cp_vec3 domain_hi, float cutoff, float lattice_h) {
+    cp_msm_layout L;
+    if (cp_msm_layout_of(n_atoms, nx, ny, nz, origin, h, domain_lo, domain_hi, cutoff, lattice_h, &L) != CP_OK)
+        return 0;
+    return L.total_bytes;
+}
+
+CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                            cp_vec3 domain_lo, cp_vec3 domain_hi, float cutoff, float lattice_h, void *workspace,
+                            size_t workspace_bytes, float *V, int accumulate, void *stream) {
+    if (!V || !workspace || (n_atoms > 0 && !atoms) || (accumulate != 0 && accumulate != 1))
+        return CP_ERR_INVALID_ARGUMENT;
+    Grid g;
+    static thread_local MsmGeom geo;
+    int rc = prepare_msm(n_atoms, nx, ny, nz, origin, h, domain_lo, domain_hi, cutoff, lattice_h, &g, &geo);
+    if (rc) return rc;
+    if (n_atoms > 0 && !aligned(atoms, 16)) return CP_ERR_MISALIGNED;
+    if (!aligned(workspace, 256) || !aligned(V, 4)) return CP_ERR_MISALIGNED;
+    if (workspace_bytes < geo.lay.total_bytes) return CP_ERR_WORKSPACE_TOO_SMALL;
+    const cp_msm_layout &L = geo.lay;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    char *cells_ws = ws + L.off_cells;
+
+    rc = sort_atoms_into_cells(reinterpret_cast<const float4 *>(atoms), n_atoms, geo.cells, geo.sortL, cells_ws, st);
+    if (rc) return rc;
+
+    MsmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.levels = L.levels;
+    p.R = L.radius;
+    p.W = reinterpret_cast<float *>(ws + L.off_stencil);
+    p.gtop = reinterpret_cast<float *>(ws + geo.off_gtop);
+    for (int d = 0; d < 3; ++d) {
+        p.cells[d] = L.cells[d];
+        p.o[d] = (&L.lattice_origin.x)[d];
+    }
+    p.h0 = lattice_h;
+    p.cell_start = reinterpret_cast<const int *>(cells_ws + geo.sortL.off_start);
+    p.cell_atoms = reinterpret_cast<const float4 *>(cells_ws + geo.sortL.off_csr_atoms);
+    p.cell_stats = reinterpret_cast<const int *>(cells_ws + geo.sortL.off_stats);
+    p.status = device_status_ptr();
+    if (!p.status) return CP_ERR_CUDA;
+    p.h0_64 = geo.h0;
+    p.a64 = geo.a;
+    p.lim2 = geo.lim2;
+    std::memcpy(p.hw, geo.hw, sizeof(p.hw));
+    long long cta = 0;
+    for (int l = 0; l < L.levels; ++l) {
+        MsmLevelDev &v = p.lv[l];
+        for (int d = 0; d < 3; ++d) {
+            v.lo[d] = L.lo[l][d];
+            v.n[d] = L.n[l][d];
+            v.qd[d] = L.q_dims[l][d];
+        }
+        v.q = reinterpret_cast<float *>(ws + L.off_q[l]);
+        v.e = reinterpret_cast<float *>(ws + L.off_e[l]);
+        v.scale = (float)std::ldexp(1.0, -l);
+        if (l + 1 < L.levels) {
+            v.part = reinterpret_cast<float *>(ws + geo.off_part[l]);
+            v.split = L.split[l];
+            v.cols = (long long)v.n[0] * v.n[1] * ((v.n[2] + kMsmZ - 1) / kMsmZ);
+            v.cta_begin = cta;
+            cta += ((v.cols + kMsmThreads - 1) / kMsmThreads) * v.split;
+        }
+    }
+    if (cta > 0x7fffffffLL) return CP_ERR_TOO_LARGE;
+    unsigned long long launches = 0;
+    const int side = 2 * L.radius + 1;
+    const long long nst = (long long)side * side * side + kMsmTopTable;
+    msm_stencil_kernel<<<(unsigned)std::min<long long>((nst + 255) / 256, 1024), 256, 0, st>>>(p);
+    const MsmLevelDev &L0 = p.lv[0];
+    const long long q0n = (long long)L0.qd[0] * L0.qd[1] * L0.qd[2];
+    msm_anterp_kernel<<<(unsigned)((q0n + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p);
+    launches += 2;
+    for (int l = 0; l + 1 < L.levels; ++l) {
+        const MsmLevelDev &C = p.lv[l + 1];
+        const long long qn = (long long)C.qd[0] * C.qd[1] * C.qd[2];
+        msm_restrict_kernel<<<(unsigned)((qn + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p, l);
+        ++launches;
+    }
+    if (cta > 0) {
+        msm_conv_kernel<<<(unsigned)cta, kMsmThreads, 0, st>>>(p);
+        ++launches;
+    }
+    const MsmLevelDev &T = p.lv[L.levels - 1];
+    const long long tn = (long long)T.n[0] * T.n[1] * T.n[2];
+    msm_top_kernel<<<(unsigned)((tn * 32 + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p);
+    ++launches;
+    for (int l = L.levels - 2; l >= 0; --l) {
+        const MsmLevelDev &F = p.lv[l];
+        const long long fn = (long long)F.n[0] * F.n[1] * F.n[2];
+        msm_reduce_prolong_kernel<<<(unsigned)((fn + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p, l);
+        ++launches;
+    }
+    InterpParams ip;
+    ip.nx = g.nx;
+    ip.ny = g.ny;
+    ip.nz = g.nz;
+    ip.ox = g.ox;
+    ip.oy = g.oy;
+    ip.oz = g.oz;
+    ip.h = g.h;
+    ip.qx = (g.nx + 3) / 4;
+    ip.quads = (long long)ip.qx * g.ny * g.nz;
+    ip.V = V;
+    ip.accumulate = accumulate;
+    const unsigned iblocks = (unsigned)((ip.quads + kMsmThreads - 1) / kMsmThreads);
+    if ((g.nx % 4 == 0) && aligned(V, 16))
+        msm_interp_kernel<true><<<iblocks, kMsmThreads, 0, st>>>(p, ip);
+    else
+        msm_interp_kernel<false><<<iblocks, kMsmThreads, 0, st>>>(p, ip);
+    ++launches;
+    if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
+    note_launches(launches);
+    return CP_OK;
+}
+
+CP_API int cp_atom_bounds(const float *atoms, int n_atoms, float *bounds, void *stream) {
+    if (!atoms || !bounds || n_atoms < 1) return CP_ERR_INVALID_ARGUMENT;
+    if (!aligned(atoms, 16) || !aligned(bounds, 4)) return CP_ERR_MISALIGNED;
+    atom_bounds_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(reinterpret_cast<const float4 *>(atoms),
+                                                                          n_atoms, bounds);
+    if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
+    note_launches(1);
+    return CP_OK;
+}
+
+}  // extern "C"

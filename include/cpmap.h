@@ -32,7 +32,8 @@
  *   V          float32 [nz][ny][nx], x fastest: V[(k*ny + j)*nx + i] (notes,
  *              section 18.4).  DEVICE pointer, 4-byte aligned (16-byte
  *              alignment and nx % 4 == 0 enable vector stores).  V is
- *              OVERWRITTEN, never accumulated into.
+ *              OVERWRITTEN, never accumulated into (the one exception is
+ *              cp_msm_longrange with accumulate = 1).
  *   stream     a cudaStream_t passed as void* (NULL = the legacy default
  *              stream).  Compute calls are asynchronous on that stream; the
  *              caller keeps every buffer alive until the stream has passed
@@ -80,6 +81,7 @@ typedef enum {
 /* Device status bits (cp_device_status). */
 #define CP_DEVICE_WAIT_TIMEOUT 0x1u /* a bounded wait on a shared-memory barrier gave up */
 #define CP_DEVICE_RANGE 0x2u        /* an index fell outside a buffer; the access was skipped */
+#define CP_DEVICE_ATOMS_OUTSIDE 0x4u /* cp_msm_longrange: an atom lay outside the domain box and was left out */
 
 /* A point or vector in Angstrom. */
 typedef struct {
@@ -310,6 +312,107 @@ CP_API size_t cp_cutoff27_workspace_bytes(int n_atoms, int nx, int ny, int nz, c
                                           float cutoff);
 CP_API int cp_cutoff27(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
                        float cutoff, void *workspace, size_t workspace_bytes, float *V, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Long-range part of a multilevel summation.
+ *
+ * The Input Binning lecture's slide "Large Bin Cut-off Kernel Code" (24)
+ * names its cutoff kernel mgpot_shortrng_energy: the switched sum of
+ * cp_cutoff is the SHORT-RANGE part of a multilevel summation of 1/r.  What
+ * it leaves out is smooth,
+ *     V_long(x) = sum_a q_a g_c(|x - r_a|),
+ *     g_c(r) = (1/c)(15/8 - 5/4 (r/c)^2 + 3/8 (r/c)^4)  for r < c,
+ *     g_c(r) = 1/r                                      for r >= c,
+ * so that cp_cutoff + V_long = the direct sum exactly.  The pages do not
+ * describe the long-range part; these calls approximate it the multilevel
+ * way (R. D. Skeel, I. Tezcan, D. J. Hardy, J. Comput. Chem. 23 (2002);
+ * D. J. Hardy, J. E. Stone, K. Schulten, Parallel Computing 35 (2009)):
+ *   lattices       level l has spacing 2^l * lattice_h; node i of every
+ *                  level sits at o + i * spacing, o = the domain's low corner;
+ *   anterpolation  charges to level-0 nodes with the C1 cubic basis
+ *                  phi(t) = (1-|t|)(1+|t|-3/2 t^2) (|t| <= 1),
+ *                  -1/2 (|t|-1)(2-|t|)^2 (1 <= |t| <= 2), 0 beyond, in each
+ *                  axis;
+ *   restriction    level l to l+1 with weights phi(i/2 - J);
+ *   lattice cutoff on level l < L, e_i = 2^-l sum_d W(d) q_{i+d} with
+ *                  W(d) = g_c(|d| h0) - g_2c(|d| h0), zero for |d| h0 >= 2c;
+ *                  on the top level L, all pairs with 2^-L g_c(|d| h0);
+ *   prolongation   e_l += the level-(l+1) potentials interpolated with
+ *                  phi(i/2 - J), from the top down;
+ *   interpolation  V_long at the grid points from level 0 with phi.
+ * Its error against the exact V_long falls like lattice_h^3 (about 1e-4 of
+ * sum_a |q_a| g_c(r) at c / lattice_h = 6).
+ *
+ * Geometry, computed on the host in fp64 from the fp32 arguments: the
+ * domain [domain_lo, domain_hi] (which must contain every atom) is widened
+ * to contain the grid; o = its low corner; level 0 has
+ * nc = floor((hi - o)/lattice_h) + 2 cells per axis (one more than the box
+ * needs, so that fp32 rounding never pushes an atom out) and nodes
+ * -1 .. nc + 1;
+ * level l+1 spans floor(lo_l/2) - 1 .. ceil(hi_l/2) + 1; the top level L
+ * is the first whose every axis has at most 12 nodes.  The stencil radius
+ * R = ceil(2c / lattice_h) must be at most CP_MSM_MAX_RADIUS.
+ *
+ * Work per call, all on the device: a counting sort of the atoms into the
+ * level-0 cells (as cp_bin_atoms), the stencil W in fp64 rounded to fp32,
+ * anterpolation (each node gathers the atoms of the 4x4x4 cells around it,
+ * in a fixed order), restriction, the lattice cutoffs of all levels in one
+ * launch (tap rows split over `split[l]` CTAs, partial sums added in a fixed
+ * order), the top level, prolongation and interpolation.  Results are
+ * deterministic.                                                           */
+#define CP_MSM_MAX_LEVELS 16
+#define CP_MSM_MAX_RADIUS 24
+
+typedef struct {
+    int levels;                        /* L + 1; level L is the dense top level */
+    int lo[CP_MSM_MAX_LEVELS][3];      /* lowest node index per axis (x, y, z) */
+    int n[CP_MSM_MAX_LEVELS][3];       /* nodes per axis */
+    int split[CP_MSM_MAX_LEVELS];      /* CTAs sharing one tile's stencil rows (levels < L) */
+    int radius;                        /* R */
+    int taps;                          /* stencil points with |d| lattice_h < 2c */
+    int cells[3];                      /* level-0 cells per axis */
+    cp_vec3 lattice_origin;            /* o (fp32) */
+    int q_dims[CP_MSM_MAX_LEVELS][3];  /* padded charge lattice: x (a multiple of 4 plus 2R), y, z */
+    size_t off_q[CP_MSM_MAX_LEVELS];   /* float32 [q_dims z][q_dims y][q_dims x]; node (i, j, k) of the
+                                        * level at [k - lo z + R][j - lo y + R][i - lo x + R], zero padding */
+    size_t off_e[CP_MSM_MAX_LEVELS];   /* lattice potentials, float32 [n z][n y][n x] */
+    size_t off_cells;                  /* the cell sort's sections start here (a cp_cutoff_layout with
+                                        * capacity 0, offsets relative to this one) */
+    size_t off_stencil;                /* W, float32 [2R+1][2R+1][2R+1] */
+    size_t off_partial;                /* partial lattice sums (internal) */
+    size_t total_bytes;                /* workspace size needed */
+} cp_msm_layout;
+
+/* Host-only: fills *out for these arguments (n_atoms >= 0).  Returns CP_OK,
+ * CP_ERR_INVALID_ARGUMENT (non-finite or non-positive cutoff or lattice_h,
+ * domain_hi < domain_lo) or CP_ERR_TOO_LARGE (R above CP_MSM_MAX_RADIUS,
+ * more than CP_MSM_MAX_LEVELS levels, a lattice or cell grid beyond the
+ * library's limits). */
+CP_API int cp_msm_layout_of(int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, cp_vec3 domain_lo,
+                            cp_vec3 domain_hi, float cutoff, float lattice_h, cp_msm_layout *out);
+
+/* Host-only: workspace bytes cp_msm_longrange needs (0 if invalid). */
+CP_API size_t cp_msm_workspace_bytes(int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                                     cp_vec3 domain_lo, cp_vec3 domain_hi, float cutoff, float lattice_h);
+
+/* V_long on the grid.  accumulate = 0 writes V = V_long; accumulate = 1
+ * adds V_long to V (after cp_cutoff with the same cutoff on the same
+ * stream, V becomes the multilevel approximation of the full direct sum).
+ * `workspace` is a DEVICE buffer of at least cp_msm_workspace_bytes(...)
+ * bytes, 256-byte aligned, owned by the caller; calls sharing it must not
+ * overlap on the GPU.  An atom outside the domain box is left out and sets
+ * CP_DEVICE_ATOMS_OUTSIDE.  Returns CP_OK, CP_ERR_INVALID_ARGUMENT,
+ * CP_ERR_MISALIGNED, CP_ERR_TOO_LARGE, CP_ERR_WORKSPACE_TOO_SMALL or
+ * CP_ERR_CUDA.                                                              */
+CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
+                            cp_vec3 domain_lo, cp_vec3 domain_hi, float cutoff, float lattice_h, void *workspace,
+                            size_t workspace_bytes, float *V, int accumulate, void *stream);
+
+/* The atoms' bounding box, for the domain of cp_msm_longrange: writes
+ * (min x, min y, min z, max x, max y, max z) as 6 floats to the DEVICE
+ * array `bounds` (4-byte aligned).  n_atoms >= 1.  Returns CP_OK,
+ * CP_ERR_INVALID_ARGUMENT, CP_ERR_MISALIGNED or CP_ERR_CUDA. */
+CP_API int cp_atom_bounds(const float *atoms, int n_atoms, float *bounds, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status and measurement helpers. */

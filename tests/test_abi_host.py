@@ -205,3 +205,59 @@ def test_cutoff_rejects_huge_cutoff_to_bin_ratio():
     assert lib.cp_offset_list(*GRID, 40.0, 1.0, None, 0, ctypes.byref(nr), ctypes.byref(nb)) == -3
     ws = ctypes.c_void_p(0x100000)
     assert lib.cp_cutoff(FAKE, 10, *GRID, 200.0, 1.0, 0, ws, 1 << 30, FAKE, None) == -3
+
+
+# ---------------------------------------------------------------------------
+# multilevel long-range part: host geometry against the oracle's rule
+
+from oracle import msm as msm_oracle  # noqa: E402
+
+MSM_CASES = [
+    # shape, origin, h, domain_lo, domain_hi, c, h0
+    ((200, 200, 200), (0.0, 0.0, 0.0), 0.5, (0.0, 0.0, 0.0), (100.0, 100.0, 100.0), 12.0, 2.0),
+    ((400, 400, 400), (0.0, 0.0, 0.0), 0.5, (0.0, 0.0, 0.0), (200.0, 200.0, 200.0), 12.0, 2.5),
+    ((37, 21, 19), (-1.0, 0.5, 2.0), 0.5, (-6.2, -4.0, -3.1), (22.0, 15.5, 16.0), 4.0, 0.7),
+    ((8, 8, 8), (0.0, 0.0, 0.0), 0.5, (0.0, 0.0, 0.0), (4.0, 4.0, 4.0), 2.0, 1.0),
+    ((30, 5, 9), (3.0, 3.0, 3.0), 0.25, (10.0, 10.0, 10.0), (11.0, 11.0, 11.0), 3.0, 0.6),  # grid outside the box
+]
+
+
+@pytest.mark.parametrize("shape,origin,h,lo,hi,c,h0", MSM_CASES)
+def test_msm_geometry_matches_oracle(shape, origin, h, lo, hi, c, h0):
+    L = cp.msm_layout(1000, shape, origin, h, c, h0, (lo, hi))
+    geo = msm_oracle.geometry(shape, origin, h, lo, hi, c, h0)
+    assert L.levels == len(geo.levels)
+    for l, lv in enumerate(geo.levels):
+        assert tuple(L.lo[l]) == lv.lo and tuple(L.n[l]) == lv.n
+    assert tuple(L.cells) == geo.cells
+    assert (L.lattice_origin.x, L.lattice_origin.y, L.lattice_origin.z) == tuple(np.float32(geo.origin))
+    W, R = msm_oracle.stencil(geo)
+    assert L.radius == R and L.taps == int((W != 0).sum())
+    assert max(L.n[L.levels - 1]) <= 12
+    assert L.total_bytes == cp.msm_workspace_bytes(1000, shape, origin, h, c, h0, (lo, hi))
+    offs = sorted([L.off_cells, L.off_stencil] + [L.off_q[l] for l in range(L.levels)] +
+                  [L.off_e[l] for l in range(L.levels)])
+    assert all(o % 256 == 0 for o in offs) and len(set(offs)) == len(offs) and offs[-1] < L.total_bytes
+    assert L.off_partial % 256 == 0 and offs[-1] < L.off_partial <= L.total_bytes  # empty with one level
+
+
+def test_msm_rejects_on_host():
+    lib = cp.library()
+    lo, hi = _lib.cp_vec3(0.0, 0.0, 0.0), _lib.cp_vec3(100.0, 100.0, 100.0)
+    args = (10, *GRID, lo, hi)
+    need = lib.cp_msm_workspace_bytes(*args, 12.0, 2.0)
+    assert need > 0
+    ws = ctypes.c_void_p(0x100000)
+    call = lambda c, h0, ws_=ws, n=need, V=FAKE, acc=0, lo_=lo, hi_=hi, atoms=FAKE: lib.cp_msm_longrange(
+        atoms, 10, *GRID, lo_, hi_, c, h0, ws_, n, V, acc, None)
+    assert call(12.0, 2.0, n=need - 1) == -4
+    assert call(12.0, 0.0) == -1 and call(-1.0, 2.0) == -1 and call(float("nan"), 2.0) == -1
+    assert call(12.0, 0.9) == -3  # stencil radius ceil(24/0.9) = 27 > 24
+    assert lib.cp_msm_workspace_bytes(*args, 12.0, 0.9) == 0
+    assert call(12.0, 2.0, hi_=_lib.cp_vec3(-1.0, 100.0, 100.0)) == -1  # domain hi < lo
+    assert call(12.0, 2.0, acc=2) == -1
+    assert call(12.0, 2.0, V=None) == -1
+    assert call(12.0, 2.0, ws_=ctypes.c_void_p(0x100010)) == -2
+    assert call(12.0, 2.0, atoms=FAKE_MIS) == -2
+    assert lib.cp_atom_bounds(FAKE, 0, FAKE, None) == -1
+    assert lib.cp_atom_bounds(FAKE_MIS, 5, FAKE, None) == -2

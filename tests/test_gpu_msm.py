@@ -1,0 +1,185 @@
+"""Parity of the multilevel long-range path (cp_msm_longrange) with the fp64
+oracle (oracle/msm.py), through the C ABI.
+
+Tolerances.  The GPU runs the oracle's steps in fp32: every lattice value is
+a sum of at most a few thousand products (7,123 stencil taps at c/h0 = 6),
+each rounded once, so its error is a small multiple of 6e-8 times the sum
+of the magnitudes it adds, far below the method's own error (about 1e-4 of
+B(x) = sum_a |q_a| g_c(|x - r_a|) at c/h0 = 6).  The tests allow
+|V_gpu - V_oracle| <= 1e-5 B(x): ten times below the method's error, so a
+wrong weight, index or level cannot hide in it.  Lattice stages are checked
+at 1e-5 of the largest value of that stage.  Against the exact sum (direct
+minus cutoff, the plain definition) the bound is the method's: 4e-4 B(x)."""
+import numpy as np
+import pytest
+import torch
+
+import direct_coulomb_summation_gb300 as cp
+import oracle
+import workloads
+from oracle import msm
+from gpu_util import flat_index
+
+pytestmark = pytest.mark.gpu
+
+CP_DEVICE_ATOMS_OUTSIDE = 0x4
+
+
+def _domain(atoms):
+    a = np.asarray(atoms, dtype=np.float32)
+    return tuple(float(v) for v in a[:, :3].min(0)), tuple(float(v) for v in a[:, :3].max(0))
+
+
+def _run(w, h0, domain=None, out=None, accumulate=False, workspace=None):
+    a = torch.from_numpy(w.atoms).cuda()
+    dom = domain if domain is not None else _domain(w.atoms)
+    V = cp.msm_longrange(a, w.shape, w.origin, w.h, w.cutoff, h0, domain=dom, out=out, accumulate=accumulate,
+                         workspace=workspace)
+    torch.cuda.synchronize()
+    return V, dom
+
+
+def _bound(w, pts=None):
+    return msm.abs_charge_bound(w.atoms, w.shape, w.origin, w.h, w.cutoff, points=pts)
+
+
+def _check(got, ref, bound, rel, name):
+    err = np.abs(got - ref)
+    worst = float((err / bound).max())
+    assert np.all(err <= rel * bound), f"{name}: max |dV|/B = {worst:.3e} > {rel:.1e}"
+
+
+CASES = [
+    # name, workload, h0
+    ("ragged", workloads.random_case(701, 700, (37, 21, 19), h=0.5, origin=(-1.0, 0.5, 2.0), margin=5.0,
+                                     cutoff=4.0, bin_size=2.0), 0.7),
+    ("offgrid_domain", workloads.random_case(702, 500, (24, 24, 24), h=0.4, origin=(3.0, -2.0, 0.0),
+                                             margin=9.0, cutoff=3.0, bin_size=1.5), 0.5),
+    ("coarse", workloads.random_case(703, 900, (30, 30, 30), h=0.5, origin=(0.0, 0.0, 0.0), margin=2.0,
+                                     cutoff=5.0, bin_size=2.5), 2.5),
+]
+
+
+@pytest.mark.parametrize("name,w,h0", CASES, ids=[c[0] for c in CASES])
+def test_longrange_matches_oracle_everywhere(name, w, h0):
+    V, dom = _run(w, h0)
+    got = V.cpu().numpy().reshape(-1).astype(np.float64)
+    ref = msm.long_range(w.atoms, w.shape, w.origin, w.h, dom[0], dom[1], w.cutoff, h0)
+    _check(got, ref, _bound(w), 1e-5, name)
+    assert cp.device_status() == 0
+
+
+def test_lattice_stages_match_oracle():
+    """q on level 0, and every level's potentials e(l), read from the workspace."""
+    name, w, h0 = CASES[0]
+    a = torch.from_numpy(w.atoms).cuda()
+    dom = _domain(w.atoms)
+    L = cp.msm_layout(len(w.atoms), w.shape, w.origin, w.h, w.cutoff, h0, dom)
+    ws = torch.empty(L.total_bytes, dtype=torch.uint8, device="cuda")
+    cp.msm_longrange(a, w.shape, w.origin, w.h, w.cutoff, h0, domain=dom, workspace=ws)
+    torch.cuda.synchronize()
+    geo = msm.geometry(w.shape, w.origin, w.h, dom[0], dom[1], w.cutoff, h0)
+    assert L.levels == len(geo.levels)
+    R = L.radius
+
+    def lattice(off, dims):
+        n = int(np.prod(dims))
+        return ws[off: off + 4 * n].view(torch.float32).view(*dims[::-1]).cpu().numpy().astype(np.float64)
+
+    q0 = lattice(L.off_q[0], tuple(L.q_dims[0]))
+    n0 = geo.levels[0].n
+    inner = q0[R:R + n0[2], R:R + n0[1], R:R + n0[0]]
+    ref_q0 = msm.anterpolate(w.atoms, geo)
+    assert np.abs(inner - ref_q0).max() <= 1e-5 * np.abs(ref_q0).max()
+    pad = q0.copy()
+    pad[R:R + n0[2], R:R + n0[1], R:R + n0[0]] = 0.0
+    assert not pad.any(), "charge lattice padding must be zero"
+    ref_e = msm.lattice_potentials(w.atoms, geo)
+    for l in range(L.levels):
+        e = lattice(L.off_e[l], tuple(L.n[l]))
+        assert np.abs(e - ref_e[l]).max() <= 1e-5 * np.abs(ref_e[l]).max(), f"level {l}"
+
+
+def test_single_level_top_only():
+    """A domain small enough that level 0 is the top (dense) level."""
+    w = workloads.random_case(704, 120, (8, 8, 8), h=0.5, origin=(0.0, 0.0, 0.0), margin=0.0, cutoff=2.0,
+                              bin_size=1.0)
+    dom = ((0.0, 0.0, 0.0), (4.0, 4.0, 4.0))
+    L = cp.msm_layout(len(w.atoms), w.shape, w.origin, w.h, w.cutoff, 1.0, dom)
+    assert L.levels == 1
+    V, _ = _run(w, 1.0, domain=dom)
+    ref = msm.long_range(w.atoms, w.shape, w.origin, w.h, dom[0], dom[1], w.cutoff, 1.0)
+    _check(V.cpu().numpy().reshape(-1).astype(np.float64), ref, _bound(w), 1e-5, "top only")
+
+
+def test_benchmark_geometry_sampled_and_full_map():
+    """200^3 map, 100k atoms, c = 12, h0 = 2 (c/h0 = 6, four levels): sampled
+    points against the oracle's multilevel sum; the multilevel map (cutoff +
+    long range) against the direct sum within the method's error."""
+    w = workloads.make("cutoff_uniform")
+    h0 = 2.0
+    a = torch.from_numpy(w.atoms).cuda()
+    dom = cp.atom_bounds(a)
+    V = cp.msm_longrange(a, w.shape, w.origin, w.h, w.cutoff, h0, domain=dom)
+    full = cp.msm_map(a, w.shape, w.origin, w.h, w.cutoff, w.bin_size, h0, capacity=0, domain=dom)
+    torch.cuda.synchronize()
+    assert cp.device_status() == 0
+    pts = workloads.sample_points(w.shape, 512, seed=7001)
+    idx = flat_index(w.shape, pts)
+    bound = _bound(w, pts)
+    ref = msm.long_range(w.atoms, w.shape, w.origin, w.h, dom[0], dom[1], w.cutoff, h0, points=pts)
+    got = V.cpu().numpy().reshape(-1).astype(np.float64)[idx]
+    _check(got, ref, bound, 1e-5, "benchmark long range")
+    vd, _ = oracle.direct(w.atoms, w.shape, w.origin, w.h, points=pts)
+    vs, _ = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, w.cutoff, points=pts)
+    _check(got, vd - vs, bound, 4e-4, "long range vs exact")
+    fm = full.cpu().numpy().reshape(-1).astype(np.float64)[idx]
+    _check(fm, vd, bound, 4e-4, "multilevel map vs direct sum")
+    assert np.all(np.isfinite(V.cpu().numpy()))
+
+
+def test_accumulate_adds_to_v():
+    name, w, h0 = CASES[0]
+    base = torch.randn(w.shape[2], w.shape[1], w.shape[0], device="cuda")
+    V1, dom = _run(w, h0)
+    V2, _ = _run(w, h0, domain=dom, out=base.clone(), accumulate=True)
+    assert torch.equal(V2, base + V1)
+
+
+def test_deterministic():
+    name, w, h0 = CASES[1]
+    V1, dom = _run(w, h0)
+    V2, _ = _run(w, h0, domain=dom)
+    assert torch.equal(V1, V2)
+
+
+def test_atom_outside_domain_is_left_out_and_flagged():
+    name, w, h0 = CASES[0]
+    dom = _domain(w.atoms)
+    far = w.atoms.copy()
+    far[5, 0] = dom[1][0] + 50.0  # outside the box given
+    a = torch.from_numpy(far).cuda()
+    V = cp.msm_longrange(a, w.shape, w.origin, w.h, w.cutoff, h0, domain=dom)
+    torch.cuda.synchronize()
+    assert cp.device_status() & CP_DEVICE_ATOMS_OUTSIDE
+    keep = np.delete(far, 5, axis=0)
+    V_ref = cp.msm_longrange(torch.from_numpy(keep).cuda(), w.shape, w.origin, w.h, w.cutoff, h0, domain=dom)
+    torch.cuda.synchronize()
+    assert cp.device_status() == 0
+    assert torch.equal(V, V_ref)
+
+
+def test_no_atoms_gives_zero():
+    w = workloads.random_case(705, 1, (12, 12, 12), h=0.5, cutoff=3.0, bin_size=1.5)
+    empty = torch.zeros((0, 4), dtype=torch.float32, device="cuda")
+    V = cp.msm_longrange(empty, w.shape, w.origin, w.h, w.cutoff, 1.0, domain=((0, 0, 0), (5.5, 5.5, 5.5)))
+    torch.cuda.synchronize()
+    assert not V.any()
+
+
+def test_atom_bounds_exact():
+    w = workloads.make("cutoff_large")
+    a = torch.from_numpy(w.atoms).cuda()
+    lo, hi = cp.atom_bounds(a)
+    assert lo == tuple(float(v) for v in w.atoms[:, :3].min(0))
+    assert hi == tuple(float(v) for v in w.atoms[:, :3].max(0))
