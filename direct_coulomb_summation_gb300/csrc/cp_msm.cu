@@ -19,10 +19,11 @@
 //   * charge lattices are stored with R zero nodes of padding on every side
 //     (z rounded up to whole 8-node columns), so the lattice-cutoff stencil
 //     reads them without bounds checks;
-//   * lattice cutoff: a thread owns 8 nodes stacked in z and walks the
-//     stencil column by column (fixed dy, dx; dz innermost), so each tap is
-//     one coalesced load of the next node of a sliding 8-node window, one
-//     uniform weight load and 8 FMAs.  All levels below the top run in one
+//   * lattice cutoff: a thread owns 8 nodes stacked in z in each of two
+//     neighbouring y columns and walks the stencil column by column (fixed
+//     dy, dx; dz innermost), so each tap is two coalesced loads (the next
+//     node of each column's sliding 8-node window), one uniform load of the
+//     weight pair (w, w) and 8 f32x2 FMAs.  All levels below the top run in one
 //     launch; the stencil columns of a tile are split over S CTAs whose
 //     partial sums are added in a fixed order afterwards;
 //   * top level: one warp per node, lanes split the other nodes, kernel
@@ -58,15 +59,14 @@ namespace {
 // ---------------------------------------------------------------------------
 // device helpers
 
-// The C1 cubic interpolating basis function, support |t| < 2.
+// The C1 cubic interpolating basis function, support |t| < 2, without
+// branches: both pieces are evaluated and the right one selected.
 __device__ __forceinline__ float msm_phi(float t) {
     const float a = fabsf(t);
-    if (a <= 1.0f) return (1.0f - a) * (1.0f + a - 1.5f * a * a);
-    if (a <= 2.0f) {
-        const float b = 2.0f - a;
-        return -0.5f * (a - 1.0f) * b * b;
-    }
-    return 0.0f;
+    const float b = 2.0f - a;
+    const float inner = (1.0f - a) * fmaf(-1.5f * a, a, 1.0f + a);
+    const float outer = -0.5f * (a - 1.0f) * b * b;
+    return a <= 1.0f ? inner : (a <= 2.0f ? outer : 0.0f);
 }
 
 // g_c(r) = gamma(r/c)/c in fp64 with explicit roundings (no contraction).
@@ -100,13 +100,15 @@ struct MsmParams {
     int levels;  // L + 1
     MsmLevelDev lv[kMsmMaxLevels];
     int R;
-    float *W;      // [2R+1]^3 stencil, symmetric in its three indices
+    float2 *W;     // [2R+1]^3 stencil as pairs (w, w), symmetric in its three indices
     float *gtop;   // top-level kernel by |d|^2
     int cells[3];
     float o[3];
     float h0;
     const int *cell_start;
     const float4 *cell_atoms;
+    float4 *cell_t;  // per cell-sorted atom: lattice coordinates (t x, t y, t z) and q
+    long long ncells;
     const int *cell_stats;
     unsigned int *status;
     double h0_64, a64, lim2;
@@ -133,7 +135,7 @@ __global__ void msm_stencil_kernel(const __grid_constant__ MsmParams p) {
                 const double r = __dmul_rn(__dsqrt_rn((double)s2), p.h0_64);
                 w = (float)__dsub_rn(msm_g64(r, p.a64), msm_g64(r, 2.0 * p.a64));
             }
-            p.W[idx] = w;
+            p.W[idx] = make_float2(w, w);
         } else {
             const int s2 = (int)(idx - n);
             const int L = p.levels - 1;
@@ -143,12 +145,23 @@ __global__ void msm_stencil_kernel(const __grid_constant__ MsmParams p) {
     }
 }
 
+// Lattice coordinates t = (r - o)/h0 of every cell-sorted atom, once per
+// atom (the same fp32 expression as the cell index), with its charge.
+__global__ void __launch_bounds__(kMsmThreads) msm_tcoord_kernel(const __grid_constant__ MsmParams p) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= p.cell_start[p.ncells]) return;
+    const float4 a = p.cell_atoms[t];
+    p.cell_t[t] = make_float4(msm_t(a.x, p.o[0], p.h0), msm_t(a.y, p.o[1], p.h0), msm_t(a.z, p.o[2], p.h0), a.w);
+}
+
 // q0 at every padded level-0 entry: zero in the padding, else the sum over
-// the atoms of the cells i-2 .. i+1 (per axis) of q Phi(t - i).
+// the atoms of the cells i-2 .. i+1 (per axis) of q Phi(t - i), in cell
+// order.
 __global__ void __launch_bounds__(kMsmThreads) msm_anterp_kernel(const __grid_constant__ MsmParams p) {
     const MsmLevelDev &L0 = p.lv[0];
     const long long total = (long long)L0.qd[0] * L0.qd[1] * L0.qd[2];
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx == 0 && p.cell_stats[1] != 0) atomicOr(p.status, CP_DEVICE_ATOMS_OUTSIDE);  // dropped by the sort
     if (idx >= total) return;
     const int px = (int)(idx % L0.qd[0]);
     const int py = (int)((idx / L0.qd[0]) % L0.qd[1]);
@@ -157,6 +170,7 @@ __global__ void __launch_bounds__(kMsmThreads) msm_anterp_kernel(const __grid_co
     float acc = 0.0f;
     if (ax >= 0 && ax < L0.n[0] && ay >= 0 && ay < L0.n[1] && az >= 0 && az < L0.n[2]) {
         const int i = ax + L0.lo[0], j = ay + L0.lo[1], k = az + L0.lo[2];  // node index
+        const float fi = (float)i, fj = (float)j, fk = (float)k;
         const int cx0 = max(i - 2, 0), cx1 = min(i + 1, p.cells[0] - 1);
         const int cy0 = max(j - 2, 0), cy1 = min(j + 1, p.cells[1] - 1);
         const int cz0 = max(k - 2, 0), cz1 = min(k + 1, p.cells[2] - 1);
@@ -166,11 +180,8 @@ __global__ void __launch_bounds__(kMsmThreads) msm_anterp_kernel(const __grid_co
                     const long long row = ((long long)cz * p.cells[1] + cy) * p.cells[0];
                     const int b = p.cell_start[row + cx0], e = p.cell_start[row + cx1 + 1];
                     for (int t = b; t < e; ++t) {
-                        const float4 a = p.cell_atoms[t];
-                        const float wx = msm_phi(msm_t(a.x, p.o[0], p.h0) - (float)i);
-                        const float wy = msm_phi(msm_t(a.y, p.o[1], p.h0) - (float)j);
-                        const float wz = msm_phi(msm_t(a.z, p.o[2], p.h0) - (float)k);
-                        acc = fmaf(a.w, wx * wy * wz, acc);
+                        const float4 a = p.cell_t[t];
+                        acc = fmaf(a.w, msm_phi(a.x - fi) * msm_phi(a.y - fj) * msm_phi(a.z - fk), acc);
                     }
                 }
         }
@@ -205,33 +216,38 @@ __global__ void __launch_bounds__(kMsmThreads) msm_restrict_kernel(const __grid_
     float acc = 0.0f;
     if (ax >= 0 && ax < C.n[0] && ay >= 0 && ay < C.n[1] && az >= 0 && az < C.n[2]) {
         const int J[3] = {ax + C.lo[0], ay + C.lo[1], az + C.lo[2]};
-        for (int kz = -3; kz <= 3; ++kz) {
-            const float wz = msm_rw(kz);
-            const int fz = 2 * J[2] + kz - F.lo[2];
-            if (wz == 0.0f || fz < 0 || fz >= F.n[2]) continue;
-            for (int ky = -3; ky <= 3; ++ky) {
-                const float wy = msm_rw(ky);
-                const int fy = 2 * J[1] + ky - F.lo[1];
-                if (wy == 0.0f || fy < 0 || fy >= F.n[1]) continue;
+        const int fx0 = 2 * J[0] - F.lo[0], fy0 = 2 * J[1] - F.lo[1], fz0 = 2 * J[2] - F.lo[2];
+        constexpr int kOff[5] = {-3, -1, 0, 1, 3};
+#pragma unroll
+        for (int c = 0; c < 5; ++c) {
+            const int fz = fz0 + kOff[c];
+            float sz = 0.0f;
+#pragma unroll
+            for (int b = 0; b < 5; ++b) {
+                const int fy = fy0 + kOff[b];
+                const bool zy_in = fz >= 0 && fz < F.n[2] && fy >= 0 && fy < F.n[1];
                 const float *row = F.q + ((long long)(fz + p.R) * F.qd[1] + (fy + p.R)) * F.qd[0] + p.R;
-                float s = 0.0f;
-                for (int kx = -3; kx <= 3; ++kx) {
-                    const float wx = msm_rw(kx);
-                    const int fx = 2 * J[0] + kx - F.lo[0];
-                    if (wx == 0.0f || fx < 0 || fx >= F.n[0]) continue;
-                    s = fmaf(wx, row[fx], s);
+                float sy = 0.0f;
+#pragma unroll
+                for (int a = 0; a < 5; ++a) {
+                    const int fx = fx0 + kOff[a];
+                    const float v = (zy_in && fx >= 0 && fx < F.n[0]) ? row[fx] : 0.0f;
+                    sy = fmaf(msm_rw(kOff[a]), v, sy);
                 }
-                acc = fmaf(wz * wy, s, acc);
+                sz = fmaf(msm_rw(kOff[b]), sy, sz);
             }
+            acc = fmaf(msm_rw(kOff[c]), sz, acc);
         }
     }
     C.q[idx] = acc;
 }
 
 // Lattice cutoff of every level below the top.  CTA -> (level, tile,
-// split); thread -> 8 nodes (x, y, z0 .. z0+7) of the level.  Split s of S
-// takes the stencil columns c = s, s + S, ...; a column (dy, dx) covers
-// dz = -hw .. hw.  The padded charge lattice makes every read in range.
+// split); thread -> node columns (x, y0) and (x, y0 + 1), 8 nodes z0 .. z0+7
+// of each, the two columns' sums held as f32x2 pairs.  Split s of S takes
+// the stencil columns c = s, s + S, ...; a column (dy, dx) covers
+// dz = -hw .. hw.  The padded charge lattice (y rounded up to even) makes
+// every read in range.
 __global__ void __launch_bounds__(kMsmThreads) msm_conv_kernel(const __grid_constant__ MsmParams p) {
     int l = 0;
     while (l + 2 < p.levels && (long long)blockIdx.x >= p.lv[l + 1].cta_begin) ++l;
@@ -241,39 +257,67 @@ __global__ void __launch_bounds__(kMsmThreads) msm_conv_kernel(const __grid_cons
     const int s = (int)(local % S);
     const long long col = (local / S) * kMsmThreads + threadIdx.x;
     if (col >= Lv.cols) return;
+    const int ny2 = (Lv.n[1] + 1) / 2;
     const int x = (int)(col % Lv.n[0]);
-    const int y = (int)((col / Lv.n[0]) % Lv.n[1]);
-    const int z0 = (int)(col / ((long long)Lv.n[0] * Lv.n[1])) * kMsmZ;
+    const int y0 = 2 * (int)((col / Lv.n[0]) % ny2);
+    const int z0 = (int)(col / ((long long)Lv.n[0] * ny2)) * kMsmZ;
     const int R = p.R, side = 2 * R + 1;
+    const int pitch = Lv.qd[0];
     const long long plane = (long long)Lv.qd[0] * Lv.qd[1];
-    const float *base = Lv.q + (long long)(z0 + R) * plane + (long long)(y + R) * Lv.qd[0] + (x + R);
-    float acc[kMsmZ];
+    const float *base = Lv.q + (long long)(z0 + R) * plane + (long long)(y0 + R) * pitch + (x + R);
+    float2 acc[kMsmZ];
 #pragma unroll
-    for (int t = 0; t < kMsmZ; ++t) acc[t] = 0.0f;
+    for (int t = 0; t < kMsmZ; ++t) acc[t] = make_float2(0.0f, 0.0f);
     const int ncols = side * side;
     for (int c = s; c < ncols; c += S) {
         const int hw = p.hw[c];
         if (hw < 0) continue;
         const int dy = c / side - R, dx = c % side - R;
-        const float *q = base + (long long)dy * Lv.qd[0] + dx;
-        const float *w = p.W + (long long)c * side + R;  // W(dy, dx, dz) at w[dz]
-        float v[kMsmZ];
+        const int taps = 2 * hw + 1;
+        // q[m * plane] = node z0 + m - hw of column (x + dx, y0 + dy); the
+        // y0 + 1 column is `pitch` further; w[m] = (W, W) at dz = m - hw
+        const float *q = base + (long long)dy * pitch + dx - (long long)hw * plane;
+        const float2 *w = p.W + (long long)c * side + R - hw;
+        // ring of 8 pairs: slot j holds the window node m' = j (mod 8), so
+        // no register moves are needed
+        float2 r[kMsmZ];
 #pragma unroll
-        for (int t = 0; t < kMsmZ - 1; ++t) v[t] = q[(long long)(t - hw) * plane];
-        for (int dz = -hw; dz <= hw; ++dz) {
-            v[kMsmZ - 1] = q[(long long)(dz + kMsmZ - 1) * plane];
-            const float wd = __ldg(w + dz);
+        for (int j = 0; j < kMsmZ - 1; ++j) {
+            r[j] = make_float2(q[0], q[pitch]);
+            q += plane;
+        }
+        int m = 0;
+        for (; m + kMsmZ <= taps; m += kMsmZ) {  // whole groups of 8 taps
 #pragma unroll
-            for (int t = 0; t < kMsmZ; ++t) acc[t] = fmaf(wd, v[t], acc[t]);
+            for (int k = 0; k < kMsmZ; ++k) {
+                r[(k + kMsmZ - 1) & (kMsmZ - 1)] = make_float2(q[0], q[pitch]);
+                q += plane;
+                const float2 wd = __ldg(w + m + k);
 #pragma unroll
-            for (int t = 0; t < kMsmZ - 1; ++t) v[t] = v[t + 1];
+                for (int t = 0; t < kMsmZ; ++t) acc[t] = __ffma2_rn(wd, r[(k + t) & (kMsmZ - 1)], acc[t]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kMsmZ - 1; ++k) {  // the remaining taps - m < 8
+            if (m + k < taps) {  // uniform across the warp
+                r[(k + kMsmZ - 1) & (kMsmZ - 1)] = make_float2(q[0], q[pitch]);
+                q += plane;
+                const float2 wd = __ldg(w + m + k);
+#pragma unroll
+                for (int t = 0; t < kMsmZ; ++t) acc[t] = __ffma2_rn(wd, r[(k + t) & (kMsmZ - 1)], acc[t]);
+            }
         }
     }
     const long long nodes = (long long)Lv.n[0] * Lv.n[1] * Lv.n[2];
-    float *out = Lv.part + (long long)s * nodes + (long long)y * Lv.n[0] + x;
+    const long long zs = (long long)Lv.n[0] * Lv.n[1];
+    float *out = Lv.part + (long long)s * nodes + (long long)y0 * Lv.n[0] + x;
+    const bool y1 = y0 + 1 < Lv.n[1];
 #pragma unroll
     for (int t = 0; t < kMsmZ; ++t)
-        if (z0 + t < Lv.n[2]) out[(long long)(z0 + t) * Lv.n[0] * Lv.n[1]] = acc[t];
+        if (z0 + t < Lv.n[2]) {
+            out[(long long)(z0 + t) * zs] = acc[t].x;
+            if (y1) out[(long long)(z0 + t) * zs + Lv.n[0]] = acc[t].y;
+        }
 }
 
 // Top level: e_i = sum_j gtop[|i - j|^2] q_j over all top nodes; one warp
@@ -286,11 +330,18 @@ __global__ void __launch_bounds__(kMsmThreads) msm_top_kernel(const __grid_const
     if (node >= nodes) return;
     const int ix = node % T.n[0], iy = (node / T.n[0]) % T.n[1], iz = node / (T.n[0] * T.n[1]);
     float acc = 0.0f;
-    for (int j = lane; j < nodes; j += 32) {
-        const int jx = j % T.n[0], jy = (j / T.n[0]) % T.n[1], jz = j / (T.n[0] * T.n[1]);
-        const int dx = ix - jx, dy = iy - jy, dz = iz - jz;
-        const float q = T.q[((long long)(jz + p.R) * T.qd[1] + (jy + p.R)) * T.qd[0] + (jx + p.R)];
-        acc = fmaf(p.gtop[dx * dx + dy * dy + dz * dz], q, acc);
+    // lane takes the top-level rows (jy, jz) = lane, lane + 32, ...; a row is
+    // summed over jx in order
+    const int rows = T.n[1] * T.n[2];
+    for (int rj = lane; rj < rows; rj += 32) {
+        const int jy = rj % T.n[1], jz = rj / T.n[1];
+        const int dy = iy - jy, dz = iz - jz;
+        const int d2 = dy * dy + dz * dz;
+        const float *q = T.q + ((long long)(jz + p.R) * T.qd[1] + (jy + p.R)) * T.qd[0] + p.R;
+        for (int jx = 0; jx < T.n[0]; ++jx) {
+            const int dx = ix - jx;
+            acc = fmaf(p.gtop[d2 + dx * dx], q[jx], acc);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, o);
@@ -366,7 +417,6 @@ template <bool VEC>
 __global__ void __launch_bounds__(kMsmThreads) msm_interp_kernel(const __grid_constant__ MsmParams p,
                                                                   const __grid_constant__ InterpParams g) {
     const long long quad = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (quad == 0 && p.cell_stats[1] != 0) atomicOr(p.status, CP_DEVICE_ATOMS_OUTSIDE);
     if (quad >= g.quads) return;
     const int qx = (int)(quad % g.qx);
     const int j = (int)((quad / g.qx) % g.ny);
@@ -456,6 +506,111 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_kernel(const __grid_co
     }
 }
 
+// Interpolation for grid spacings h <= h0: one CTA per 8x8x8-point brick.
+// The brick's points need at most kSpan level-0 nodes per axis; those are
+// staged in shared memory and the tensor-product sum is done one axis at a
+// time (z, then y, then x), so a point costs about 12 FMAs instead of 64.
+constexpr int kInterpSpan = 12;
+
+__global__ void __launch_bounds__(kMsmThreads) msm_interp_brick_kernel(const __grid_constant__ MsmParams p,
+                                                                        const __grid_constant__ InterpParams g) {
+    __shared__ float E[kInterpSpan][kInterpSpan][kInterpSpan];  // [z][y][x] nodes around the brick
+    __shared__ float S1[kBrick][kInterpSpan][kInterpSpan];      // [point z][node y][node x]
+    __shared__ float S2[kBrick][kBrick][kInterpSpan];           // [point z][point y][node x]
+    __shared__ float wgt[3][kBrick][4];
+    __shared__ int off[3][kBrick];
+    __shared__ int base[3], cnt[3];
+    __shared__ int bad;
+
+    const int tid = threadIdx.x;
+    const int nbx = (g.nx + kBrick - 1) / kBrick, nby = (g.ny + kBrick - 1) / kBrick;
+    const int bx = blockIdx.x % nbx, by = (blockIdx.x / nbx) % nby, bz = blockIdx.x / (nbx * nby);
+    const MsmLevelDev &L0 = p.lv[0];
+    if (tid == 0) bad = 0;
+    if (tid < 3 * kBrick) {
+        // per axis d and point p of the brick: node offset and the 4 weights
+        const int d = tid / kBrick, pt = tid % kBrick;
+        const int n = d == 0 ? g.nx : (d == 1 ? g.ny : g.nz);
+        const int b = d == 0 ? bx : (d == 1 ? by : bz);
+        const float o = d == 0 ? g.ox : (d == 1 ? g.oy : g.oz);
+        const int idx = min(kBrick * b + pt, n - 1);  // points past the edge repeat the last one
+        const float t = msm_t(fmaf((float)idx, g.h, o), p.o[d], p.h0);
+        const int k = min(max((int)floorf(t), 0), p.cells[d] - 1);
+        const int idx0 = kBrick * b;
+        const float t0 = msm_t(fmaf((float)idx0, g.h, o), p.o[d], p.h0);
+        const int k0 = min(max((int)floorf(t0), 0), p.cells[d] - 1);
+        off[d][pt] = k - k0;
+        for (int a = 0; a < 4; ++a) wgt[d][pt][a] = msm_phi(t - (float)(k - 1 + a));
+        if (pt == kBrick - 1) {
+            base[d] = k0 - 1 - L0.lo[d];  // array index of the first node
+            cnt[d] = k - k0 + 4;
+            if (k - k0 + 4 > kInterpSpan || k < k0) atomicOr(&bad, 1);
+        }
+    }
+    __syncthreads();
+    if (bad) {  // cannot happen for h <= h0; recorded rather than trusted
+        if (tid == 0) atomicOr(p.status, CP_DEVICE_RANGE);
+        return;
+    }
+    const int cx = cnt[0], cy = cnt[1], cz = cnt[2];
+    for (int e = tid; e < cx * cy * cz; e += kMsmThreads) {
+        const int ex = e % cx, ey = (e / cx) % cy, ez = e / (cx * cy);
+        const int gx = base[0] + ex, gy = base[1] + ey, gz = base[2] + ez;
+        const bool in = gx >= 0 && gx < L0.n[0] && gy >= 0 && gy < L0.n[1] && gz >= 0 && gz < L0.n[2];
+        E[ez][ey][ex] = in ? L0.e[((long long)gz * L0.n[1] + gy) * L0.n[0] + gx] : 0.0f;
+    }
+    __syncthreads();
+    for (int e = tid; e < kBrick * cy * cx; e += kMsmThreads) {  // along z
+        const int ex = e % cx, ey = (e / cx) % cy, pz = e / (cx * cy);
+        const int o = off[2][pz];
+        float v = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v = fmaf(wgt[2][pz][c], E[o + c][ey][ex], v);
+        S1[pz][ey][ex] = v;
+    }
+    __syncthreads();
+    for (int e = tid; e < kBrick * kBrick * cx; e += kMsmThreads) {  // along y
+        const int ex = e % cx, py = (e / cx) % kBrick, pz = e / (cx * kBrick);
+        const int o = off[1][py];
+        float v = 0.0f;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) v = fmaf(wgt[1][py][b], S1[pz][o + b][ex], v);
+        S2[pz][py][ex] = v;
+    }
+    __syncthreads();
+    // along x: thread -> 4 consecutive points of one brick row
+    const int half = tid & 1, py = (tid >> 1) & (kBrick - 1), pz = tid >> 4;
+    float v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int px = 4 * half + c;
+        const int o = off[0][px];
+        float s = 0.0f;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) s = fmaf(wgt[0][px][a], S2[pz][py][o + a], s);
+        v[c] = s;
+    }
+    const int i0 = kBrick * bx + 4 * half, j = kBrick * by + py, k = kBrick * bz + pz;
+    if (j >= g.ny || k >= g.nz) return;
+    float *row = g.V + ((long long)k * g.ny + j) * g.nx;
+    if (i0 + 3 < g.nx && (g.nx % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.V) & 15) == 0)) {
+        float4 *dst = reinterpret_cast<float4 *>(row + i0);
+        float4 out = make_float4(v[0], v[1], v[2], v[3]);
+        if (g.accumulate) {
+            const float4 old = *dst;
+            out.x += old.x;
+            out.y += old.y;
+            out.z += old.z;
+            out.w += old.w;
+        }
+        *dst = out;
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (i0 + c < g.nx) row[i0 + c] = g.accumulate ? row[i0 + c] + v[c] : v[c];
+    }
+}
+
 // Bounding box of the atoms, one CTA: per-thread min/max, then a tree
 // reduction in shared memory (min and max do not depend on the order).
 __global__ void __launch_bounds__(1024) atom_bounds_kernel(const float4 *atoms, int n, float *out) {
@@ -498,6 +653,7 @@ struct MsmGeom {
     cp_cutoff_layout sortL;
     size_t off_gtop;
     size_t off_part[kMsmMaxLevels];
+    size_t off_tcoord;
     int8_t hw[kMsmSide * kMsmSide];
 };
 
@@ -583,13 +739,13 @@ int make_msm_geometry(int n_atoms, const Grid &g, cp_vec3 dlo, cp_vec3 dhi, floa
     L.off_cells = off;
     off = align256(off + out->sortL.total_bytes);
     L.off_stencil = off;
-    off = align256(off + 4 * (size_t)side * side * side);
+    off = align256(off + 8 * (size_t)side * side * side);
     out->off_gtop = off;
     off = align256(off + 4 * (size_t)kMsmTopTable);
     for (int l = 0; l < levels; ++l) {
         const long long n0 = L.n[l][0], n1 = L.n[l][1], n2 = L.n[l][2];
         L.q_dims[l][0] = (int)n0 + 2 * R;
-        L.q_dims[l][1] = (int)n1 + 2 * R;
+        L.q_dims[l][1] = (int)(2 * ((n1 + 1) / 2)) + 2 * R;
         L.q_dims[l][2] = (int)(kMsmZ * ((n2 + kMsmZ - 1) / kMsmZ)) + 2 * R;
         const long long qn = (long long)L.q_dims[l][0] * L.q_dims[l][1] * L.q_dims[l][2];
         if (qn > INT_MAX) return CP_ERR_TOO_LARGE;
@@ -600,12 +756,14 @@ int make_msm_geometry(int n_atoms, const Grid &g, cp_vec3 dlo, cp_vec3 dhi, floa
     }
     L.off_partial = off;
     for (int l = 0; l + 1 < levels; ++l) {
-        const long long cols = (long long)L.n[l][0] * L.n[l][1] * ((L.n[l][2] + kMsmZ - 1) / kMsmZ);
+        const long long cols = (long long)L.n[l][0] * ((L.n[l][1] + 1) / 2) * ((L.n[l][2] + kMsmZ - 1) / kMsmZ);
         const long long want = (kMsmTargetThreads + cols - 1) / cols;
         L.split[l] = (int)std::max(1LL, std::min<long long>({want, (long long)kMsmMaxSplit, (long long)ncols}));
         out->off_part[l] = off;
         off = align256(off + 4 * (size_t)L.split[l] * (size_t)(L.n[l][0] * L.n[l][1] * L.n[l][2]));
     }
+    out->off_tcoord = off;
+    off = align256(off + 16 * (size_t)n_atoms);
     L.total_bytes = off;
     return CP_OK;
 }
@@ -668,7 +826,7 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     std::memset(&p, 0, sizeof(p));
     p.levels = L.levels;
     p.R = L.radius;
-    p.W = reinterpret_cast<float *>(ws + L.off_stencil);
+    p.W = reinterpret_cast<float2 *>(ws + L.off_stencil);
     p.gtop = reinterpret_cast<float *>(ws + geo.off_gtop);
     for (int d = 0; d < 3; ++d) {
         p.cells[d] = L.cells[d];
@@ -678,6 +836,8 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     p.cell_start = reinterpret_cast<const int *>(cells_ws + geo.sortL.off_start);
     p.cell_atoms = reinterpret_cast<const float4 *>(cells_ws + geo.sortL.off_csr_atoms);
     p.cell_stats = reinterpret_cast<const int *>(cells_ws + geo.sortL.off_stats);
+    p.cell_t = reinterpret_cast<float4 *>(ws + geo.off_tcoord);
+    p.ncells = geo.cells.nbins;
     p.status = device_status_ptr();
     if (!p.status) return CP_ERR_CUDA;
     p.h0_64 = geo.h0;
@@ -698,7 +858,7 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
         if (l + 1 < L.levels) {
             v.part = reinterpret_cast<float *>(ws + geo.off_part[l]);
             v.split = L.split[l];
-            v.cols = (long long)v.n[0] * v.n[1] * ((v.n[2] + kMsmZ - 1) / kMsmZ);
+            v.cols = (long long)v.n[0] * ((v.n[1] + 1) / 2) * ((v.n[2] + kMsmZ - 1) / kMsmZ);
             v.cta_begin = cta;
             cta += ((v.cols + kMsmThreads - 1) / kMsmThreads) * v.split;
         }
@@ -710,6 +870,10 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     msm_stencil_kernel<<<(unsigned)std::min<long long>((nst + 255) / 256, 1024), 256, 0, st>>>(p);
     const MsmLevelDev &L0 = p.lv[0];
     const long long q0n = (long long)L0.qd[0] * L0.qd[1] * L0.qd[2];
+    if (n_atoms > 0) {
+        msm_tcoord_kernel<<<(unsigned)((n_atoms + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p);
+        ++launches;
+    }
     msm_anterp_kernel<<<(unsigned)((q0n + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p);
     launches += 2;
     for (int l = 0; l + 1 < L.levels; ++l) {
@@ -745,7 +909,11 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     ip.V = V;
     ip.accumulate = accumulate;
     const unsigned iblocks = (unsigned)((ip.quads + kMsmThreads - 1) / kMsmThreads);
-    if ((g.nx % 4 == 0) && aligned(V, 16))
+    const long long nbricks = (long long)((g.nx + kBrick - 1) / kBrick) * ((g.ny + kBrick - 1) / kBrick) *
+                              ((g.nz + kBrick - 1) / kBrick);
+    if (g.h <= lattice_h && nbricks <= 0x7fffffffLL)
+        msm_interp_brick_kernel<<<(unsigned)nbricks, kMsmThreads, 0, st>>>(p, ip);
+    else if ((g.nx % 4 == 0) && aligned(V, 16))
         msm_interp_kernel<true><<<iblocks, kMsmThreads, 0, st>>>(p, ip);
     else
         msm_interp_kernel<false><<<iblocks, kMsmThreads, 0, st>>>(p, ip);

@@ -372,13 +372,14 @@ typedef struct {
     int taps;                          /* stencil points with |d| lattice_h < 2c */
     int cells[3];                      /* level-0 cells per axis */
     cp_vec3 lattice_origin;            /* o (fp32) */
-    int q_dims[CP_MSM_MAX_LEVELS][3];  /* padded charge lattice: x (a multiple of 4 plus 2R), y, z */
+    int q_dims[CP_MSM_MAX_LEVELS][3];  /* padded charge lattice: x + 2R, y rounded up to even + 2R,
+                                        * z rounded up to a multiple of 8 + 2R */
     size_t off_q[CP_MSM_MAX_LEVELS];   /* float32 [q_dims z][q_dims y][q_dims x]; node (i, j, k) of the
                                         * level at [k - lo z + R][j - lo y + R][i - lo x + R], zero padding */
     size_t off_e[CP_MSM_MAX_LEVELS];   /* lattice potentials, float32 [n z][n y][n x] */
     size_t off_cells;                  /* the cell sort's sections start here (a cp_cutoff_layout with
                                         * capacity 0, offsets relative to this one) */
-    size_t off_stencil;                /* W, float32 [2R+1][2R+1][2R+1] */
+    size_t off_stencil;                /* W as float32 pairs (w, w), [2R+1][2R+1][2R+1] */
     size_t off_partial;                /* partial lattice sums (internal) */
     size_t total_bytes;                /* workspace size needed */
 } cp_msm_layout;
