@@ -421,6 +421,43 @@ def run_ours(args):
             torch.cuda.synchronize()
             tg.append(e0.elapsed_time(e1))
         t_graph_cut = float(np.mean(tg)) / 1e3
+    # multilevel long-range part on the cutoff workload (reported beside the
+    # step, not part of it): cp_msm_longrange adding V_long to the cutoff map
+    msm = None
+    if do_cutoff and not args.no_msm:
+        lo, hi = cp.atom_bounds(ac)
+        dom = (cp._vec3(lo), cp._vec3(hi))
+        h0 = float(np.float32(args.msm_lattice))
+        ML = cp.msm_layout(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, h0, (lo, hi))
+        mws = torch.empty(int(ML.total_bytes), dtype=torch.uint8, device=device)
+
+        def run_msm():
+            call(lib.cp_msm_longrange(ac.data_ptr(), wc.n_atoms, *gc, *dom, cut[0], h0, mws.data_ptr(),
+                                      int(ML.total_bytes), Vc.data_ptr(), 1, sh), "cp_msm_longrange")
+
+        for _ in range(3):
+            run_msm()
+        torch.cuda.synchronize()
+        n_msm = max(3, min(args.steps, 20))
+        tm = []
+        m_launch0 = lib.cp_launch_count()
+        for _ in range(n_msm):
+            flush.fill_(7)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run_msm()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            tm.append(e0.elapsed_time(e1))
+        m_launches = (lib.cp_launch_count() - m_launch0) // n_msm
+        levels = int(ML.levels)
+        nodes = [int(ML.n[l][0]) * int(ML.n[l][1]) * int(ML.n[l][2]) for l in range(levels)]
+        # algorithmic FMAs of the lattice cutoffs: every node of every level
+        # below the top times the stencil's taps, plus the dense top level
+        fma = sum(nodes[:-1]) * int(ML.taps) + nodes[-1] ** 2
+        msm = {"lattice_h": h0, "levels": levels, "nodes": nodes, "stencil_taps": int(ML.taps),
+               "ms_longrange": float(np.median(tm)), "launches_per_call": int(m_launches),
+               "lattice_cutoff_fma_per_call": fma}
     status = cp.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status:#x} after the timed steps")
@@ -565,6 +602,16 @@ def run_ours(args):
                 "algorithmic_bytes": bin_bytes, "peak_basis": f"hbm_gbs {hbm_basis}",
             },
         },
+        "msm": None if msm is None else dict(
+            msm,
+            ms_map=1e3 * t_cut / K + msm["ms_longrange"],
+            grid_points_per_s_map=float(wc.n_points) * world / (t_cut / K + 1e-3 * msm["ms_longrange"]),
+            fp32_fma_per_s_longrange=msm["lattice_cutoff_fma_per_call"] / (1e-3 * msm["ms_longrange"]),
+            frac_of_fp32_fma=msm["lattice_cutoff_fma_per_call"] / (1e-3 * msm["ms_longrange"]) / (r_ffma * sm_clk / world),
+            basis="the whole cp_msm_longrange call (cell sort, anterpolation, restriction, lattice cutoffs, "
+                  "prolongation, interpolation) against the FP32 FMA rate for its lattice-cutoff FMAs alone; "
+                  "ms_map adds the cutoff leg (binning + short-range map): the multilevel approximation of the "
+                  "full direct sum on this grid"),
         "cpu_baseline": cpu,
         "e2e": {
             "value": float(wd.n_pairs) * world / t_e2e_d,
@@ -675,6 +722,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-msm", action="store_true", help="skip the multilevel long-range measurement")
+    ap.add_argument("--msm-lattice", type=float, default=2.0, help="finest lattice spacing of the long-range part")
     ap.add_argument("--only", choices=["both", "direct", "cutoff"], default="both",
                     help="time one leg only (for profiling; the JSON line then covers that leg)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")

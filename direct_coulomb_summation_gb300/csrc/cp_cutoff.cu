@@ -231,6 +231,80 @@ __global__ void __launch_bounds__(256) bin_sort_pack_kernel(const __grid_constan
     }
 }
 
+// The same per-bin sort and pack for bin grids whose bins hold few atoms
+// (lattice cells): lane b of a warp owns bin 32*warp + b and ranks a bin of
+// at most kLaneSortMax atoms by itself; larger bins are ranked by the whole
+// warp, one after another.  Results are identical to bin_sort_pack_kernel.
+constexpr int kLaneSortMax = 16;
+
+__global__ void __launch_bounds__(256) bin_sort_pack_lane_kernel(const __grid_constant__ BinParams p) {
+    __shared__ int blk_overflow, blk_max;
+    if (threadIdx.x == 0) {
+        blk_overflow = 0;
+        blk_max = 0;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int bin0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * 32;
+    const int bin = bin0 + lane;
+    const bool valid = bin < p.nbins;
+    const int n = valid ? p.count[bin] : 0;
+    const int s = valid ? p.start[bin] + p.block_prefix[bin / kScanBlock] : 0;
+    int *tmp = reinterpret_cast<int *>(p.bin_rank);  // free after the scatter
+    const bool small = n <= kLaneSortMax;
+    if (valid && small) {
+        for (int c0 = 0; c0 < n; ++c0) {
+            const int e = p.csr_index[s + c0];
+            int rank = 0;
+            for (int c1 = 0; c1 < n; ++c1) rank += (p.csr_index[s + c1] < e) ? 1 : 0;
+            const float4 a = p.atoms[e];
+            tmp[s + rank] = e;
+            p.csr_atoms[s + rank] = a;
+            if (rank < p.K) p.padded[(long long)bin * p.K + rank] = a;
+        }
+    }
+    unsigned big = __ballot_sync(0xffffffffu, valid && !small);
+    while (big != 0u) {
+        const int lb = __ffs(big) - 1;
+        big &= big - 1u;
+        const int bn = __shfl_sync(0xffffffffu, n, lb);
+        const int bs = __shfl_sync(0xffffffffu, s, lb);
+        const int bb = bin0 + lb;
+        for (int c0 = 0; c0 < bn; c0 += 32) {
+            const int e = (c0 + lane < bn) ? p.csr_index[bs + c0 + lane] : INT_MAX;
+            int rank = 0;
+            for (int c1 = 0; c1 < bn; c1 += 32) {
+                const int f = (c1 + lane < bn) ? p.csr_index[bs + c1 + lane] : INT_MAX;
+                const int m = min(32, bn - c1);
+                for (int k = 0; k < m; ++k) rank += (__shfl_sync(0xffffffffu, f, k) < e) ? 1 : 0;
+            }
+            if (c0 + lane < bn) {
+                const float4 a = p.atoms[e];
+                tmp[bs + rank] = e;
+                p.csr_atoms[bs + rank] = a;
+                if (rank < p.K) p.padded[(long long)bb * p.K + rank] = a;
+            }
+        }
+        __syncwarp();
+        for (int k = lane; k < bn; k += 32) p.csr_index[bs + k] = tmp[bs + k];
+        __syncwarp();
+    }
+    if (valid) {
+        if (small) {
+            for (int k = 0; k < n; ++k) p.csr_index[s + k] = tmp[s + k];
+            for (int k = n; k < p.K; ++k) p.padded[(long long)bin * p.K + k] = make_float4(kPadCoord, kPadCoord, kPadCoord, 0.0f);
+        }
+        p.start[bin] = s;
+        if (n > p.K) atomicAdd(&blk_overflow, n - p.K);
+        atomicMax(&blk_max, n);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (blk_overflow) atomicAdd(&p.stats[2], blk_overflow);
+        atomicMax(&p.stats[3], blk_max);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // brick kernel
 
@@ -576,7 +650,7 @@ BinParams bin_params(const float4 *atoms, int n_atoms, const BinGeom &bg, const 
     return b;
 }
 
-int launch_binning_params(const BinParams &b, cudaStream_t stream) {
+int launch_binning_params(const BinParams &b, cudaStream_t stream, bool small_bins = false) {
     const int nblk = (int)(((long long)b.nbins + kScanBlock - 1) / kScanBlock);
     DeviceInfo dev;
     int rc = device_info(&dev);
@@ -587,7 +661,10 @@ int launch_binning_params(const BinParams &b, cudaStream_t stream) {
     bin_scan_local_kernel<<<nblk, 256, 0, stream>>>(b);
     bin_scan_blocks_kernel<<<1, 1024, 0, stream>>>(b, nblk);
     if (b.n > 0) bin_scatter_kernel<<<(b.n + 255) / 256, 256, 0, stream>>>(b);
-    bin_sort_pack_kernel<<<(b.nbins + 7) / 8, 256, 0, stream>>>(b);
+    if (small_bins)
+        bin_sort_pack_lane_kernel<<<(b.nbins + 255) / 256, 256, 0, stream>>>(b);
+    else
+        bin_sort_pack_kernel<<<(b.nbins + 7) / 8, 256, 0, stream>>>(b);
     if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
     note_launches(b.n > 0 ? 6 : 4);
     return CP_OK;
@@ -688,7 +765,7 @@ int launch_bricks(const Prepared &P, const OffsetList &L, float *V, cudaStream_t
 int sort_atoms_into_cells(const float4 *atoms, int n_atoms, const BinGeom &bg, const cp_cutoff_layout &L,
                           void *workspace, cudaStream_t stream) {
     if (L.capacity != 0 || L.nbins != bg.nbins) return CP_ERR_INVALID_ARGUMENT;
-    return launch_binning_params(bin_params(atoms, n_atoms, bg, L, workspace), stream);
+    return launch_binning_params(bin_params(atoms, n_atoms, bg, L, workspace), stream, true);
 }
 
 }  // namespace cpmap

@@ -376,6 +376,7 @@ __global__ void __launch_bounds__(kMsmThreads) msm_reduce_prolong_kernel(const _
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= nodes) return;
     float s = 0.0f;
+#pragma unroll 8
     for (int k = 0; k < F.split; ++k) s += F.part[(long long)k * nodes + idx];
     const int ax = (int)(idx % F.n[0]);
     const int ay = (int)((idx / F.n[0]) % F.n[1]);
