@@ -61,6 +61,7 @@ class cp_msm_layout(ctypes.Structure):
         ("cells", ctypes.c_int * 3),
         ("lattice_origin", cp_vec3),
         ("q_dims", (ctypes.c_int * 3) * MSM_MAX_LEVELS),
+        ("q_plane", ctypes.c_int * MSM_MAX_LEVELS),
         ("off_q", ctypes.c_size_t * MSM_MAX_LEVELS),
         ("off_e", ctypes.c_size_t * MSM_MAX_LEVELS),
         ("off_cells", ctypes.c_size_t),

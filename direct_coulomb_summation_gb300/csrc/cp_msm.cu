@@ -21,9 +21,11 @@
 //     reads them without bounds checks;
 //   * lattice cutoff: a thread owns 8 nodes stacked in z in each of two
 //     neighbouring y columns and walks the stencil column by column (fixed
-//     dy, dx; dz innermost), so each tap is two coalesced loads (the next
-//     node of each column's sliding 8-node window), one uniform load of the
-//     weight pair (w, w) and 8 f32x2 FMAs.  All levels below the top run in one
+//     dy, dx; dz innermost).  Charge lattices store each node with its +y
+//     neighbour, (q(x,y,z), q(x,y+1,z)), and a power-of-two z stride that
+//     is a compile-time constant, so each tap is one coalesced 8-byte load
+//     at an immediate offset (the next pair of a sliding 8-node window),
+//     one uniform load of the weight pair (w, w) and 8 f32x2 FMAs.  All levels below the top run in one
 //     launch; the stencil columns of a tile are split over S CTAs whose
 //     partial sums are added in a fixed order afterwards;
 //   * top level: one warp per node, lanes split the other nodes, kernel
@@ -53,6 +55,8 @@ constexpr int kMsmZ = 8;                                      // nodes a lattice
 constexpr long long kMsmTargetThreads = 1LL << 17;            // lattice-cutoff threads worth splitting for
 constexpr int kMsmMaxSplit = 64;
 constexpr int kMsmThreads = 128;
+constexpr long long kMsmMinPlane = 1024;     // z-plane strides of the charge lattices: powers of two
+constexpr long long kMsmMaxPlane = 1 << 18;  // in this range, each a compile-time constant of the stencil loop
 
 namespace {
 
@@ -87,7 +91,8 @@ __device__ __forceinline__ float msm_t(float x, float o, float h0) { return __fd
 struct MsmLevelDev {
     int lo[3], n[3];
     int qd[3];              // padded charge lattice dims (x, y, z)
-    float *q;               // padded charges
+    float2 *q;              // padded charges as pairs (q(x,y,z), q(x,y+1,z)), [z][plane]
+    int plane;              // entries per z plane: a power of two >= qd[0] * qd[1]
     float *e;               // potentials [n z][n y][n x]
     float *part;            // partial sums [split][n z][n y][n x]
     int split;
@@ -114,6 +119,17 @@ struct MsmParams {
     double h0_64, a64, lim2;
     int8_t hw[kMsmSide * kMsmSide];  // stencil column (dy, dx) half height in dz, -1 if empty
 };
+
+// Writes charge q of padded entry (x, y, z): as the first half of its own
+// pair and the second half of the pair of (x, y-1, z); the last row's
+// second halves (beyond the lattice) are zero.
+__device__ __forceinline__ void msm_store_pair(const MsmLevelDev &L, int x, int y, int z, float q) {
+    float2 *base = L.q + (long long)z * L.plane + x;
+    float *own = reinterpret_cast<float *>(base + (long long)y * L.qd[0]);
+    own[0] = q;
+    if (y > 0) own[1 - 2 * L.qd[0]] = q;  // .y of the entry one row down
+    if (y == L.qd[1] - 1) own[1] = 0.0f;
+}
 
 // ---------------------------------------------------------------------------
 // kernels
@@ -186,7 +202,7 @@ __global__ void __launch_bounds__(kMsmThreads) msm_anterp_kernel(const __grid_co
                 }
         }
     }
-    L0.q[idx] = acc;
+    msm_store_pair(L0, px, py, pz, acc);
 }
 
 // Restriction weights phi(k/2) for fine offsets k = -3 .. 3 (k = +-2 weigh 0).
@@ -226,12 +242,12 @@ __global__ void __launch_bounds__(kMsmThreads) msm_restrict_kernel(const __grid_
             for (int b = 0; b < 5; ++b) {
                 const int fy = fy0 + kOff[b];
                 const bool zy_in = fz >= 0 && fz < F.n[2] && fy >= 0 && fy < F.n[1];
-                const float *row = F.q + ((long long)(fz + p.R) * F.qd[1] + (fy + p.R)) * F.qd[0] + p.R;
+                const float2 *row = F.q + (long long)(fz + p.R) * F.plane + (long long)(fy + p.R) * F.qd[0] + p.R;
                 float sy = 0.0f;
 #pragma unroll
                 for (int a = 0; a < 5; ++a) {
                     const int fx = fx0 + kOff[a];
-                    const float v = (zy_in && fx >= 0 && fx < F.n[0]) ? row[fx] : 0.0f;
+                    const float v = (zy_in && fx >= 0 && fx < F.n[0]) ? row[fx].x : 0.0f;
                     sy = fmaf(msm_rw(kOff[a]), v, sy);
                 }
                 sz = fmaf(msm_rw(kOff[b]), sy, sz);
@@ -239,70 +255,62 @@ __global__ void __launch_bounds__(kMsmThreads) msm_restrict_kernel(const __grid_
             acc = fmaf(msm_rw(kOff[c]), sz, acc);
         }
     }
-    C.q[idx] = acc;
+    msm_store_pair(C, px, py, pz, acc);
 }
 
 // Lattice cutoff of every level below the top.  CTA -> (level, tile,
 // split); thread -> node columns (x, y0) and (x, y0 + 1), 8 nodes z0 .. z0+7
 // of each, the two columns' sums held as f32x2 pairs.  Split s of S takes
 // the stencil columns c = s, s + S, ...; a column (dy, dx) covers
-// dz = -hw .. hw.  The padded charge lattice (y rounded up to even) makes
-// every read in range.
-__global__ void __launch_bounds__(kMsmThreads) msm_conv_kernel(const __grid_constant__ MsmParams p) {
-    int l = 0;
-    while (l + 2 < p.levels && (long long)blockIdx.x >= p.lv[l + 1].cta_begin) ++l;
-    const MsmLevelDev &Lv = p.lv[l];
-    const long long local = (long long)blockIdx.x - Lv.cta_begin;
-    const int S = Lv.split;
-    const int s = (int)(local % S);
-    const long long col = (local / S) * kMsmThreads + threadIdx.x;
-    if (col >= Lv.cols) return;
+// dz = -hw .. hw.  Each charge entry holds the pair (q(x,y,z), q(x,y+1,z)),
+// so a tap is one 8-byte load; PLANE (the z stride) is a compile-time
+// constant, so the loads of an unrolled group of 8 taps use immediate
+// offsets.  The padded charge lattice makes every read in range.
+template <int PLANE>
+__device__ __forceinline__ void msm_conv_tile(const MsmParams &p, const MsmLevelDev &Lv, int s, long long col) {
     const int ny2 = (Lv.n[1] + 1) / 2;
     const int x = (int)(col % Lv.n[0]);
     const int y0 = 2 * (int)((col / Lv.n[0]) % ny2);
     const int z0 = (int)(col / ((long long)Lv.n[0] * ny2)) * kMsmZ;
     const int R = p.R, side = 2 * R + 1;
     const int pitch = Lv.qd[0];
-    const long long plane = (long long)Lv.qd[0] * Lv.qd[1];
-    const float *base = Lv.q + (long long)(z0 + R) * plane + (long long)(y0 + R) * pitch + (x + R);
+    const float2 *base = Lv.q + (long long)(z0 + R) * PLANE + (long long)(y0 + R) * pitch + (x + R);
     float2 acc[kMsmZ];
 #pragma unroll
     for (int t = 0; t < kMsmZ; ++t) acc[t] = make_float2(0.0f, 0.0f);
     const int ncols = side * side;
-    for (int c = s; c < ncols; c += S) {
+    for (int c = s; c < ncols; c += Lv.split) {
         const int hw = p.hw[c];
         if (hw < 0) continue;
         const int dy = c / side - R, dx = c % side - R;
         const int taps = 2 * hw + 1;
-        // q[m * plane] = node z0 + m - hw of column (x + dx, y0 + dy); the
-        // y0 + 1 column is `pitch` further; w[m] = (W, W) at dz = m - hw
-        const float *q = base + (long long)dy * pitch + dx - (long long)hw * plane;
-        const float2 *w = p.W + (long long)c * side + R - hw;
+        // q[m * PLANE] = node pair z0 + m - hw of column (x + dx, y0 + dy);
+        // w[m] = (W, W) at dz = m - hw
+        const float2 *q = base + dy * pitch + dx - hw * PLANE;
+        const float2 *w = p.W + c * side + R - hw;
         // ring of 8 pairs: slot j holds the window node m' = j (mod 8), so
         // no register moves are needed
         float2 r[kMsmZ];
 #pragma unroll
-        for (int j = 0; j < kMsmZ - 1; ++j) {
-            r[j] = make_float2(q[0], q[pitch]);
-            q += plane;
-        }
+        for (int j = 0; j < kMsmZ - 1; ++j) r[j] = q[j * PLANE];
+        q += (kMsmZ - 1) * PLANE;
         int m = 0;
         for (; m + kMsmZ <= taps; m += kMsmZ) {  // whole groups of 8 taps
 #pragma unroll
             for (int k = 0; k < kMsmZ; ++k) {
-                r[(k + kMsmZ - 1) & (kMsmZ - 1)] = make_float2(q[0], q[pitch]);
-                q += plane;
-                const float2 wd = __ldg(w + m + k);
+                r[(k + kMsmZ - 1) & (kMsmZ - 1)] = q[k * PLANE];
+                const float2 wd = __ldg(w + k);
 #pragma unroll
                 for (int t = 0; t < kMsmZ; ++t) acc[t] = __ffma2_rn(wd, r[(k + t) & (kMsmZ - 1)], acc[t]);
             }
+            q += kMsmZ * PLANE;
+            w += kMsmZ;
         }
 #pragma unroll
         for (int k = 0; k < kMsmZ - 1; ++k) {  // the remaining taps - m < 8
             if (m + k < taps) {  // uniform across the warp
-                r[(k + kMsmZ - 1) & (kMsmZ - 1)] = make_float2(q[0], q[pitch]);
-                q += plane;
-                const float2 wd = __ldg(w + m + k);
+                r[(k + kMsmZ - 1) & (kMsmZ - 1)] = q[k * PLANE];
+                const float2 wd = __ldg(w + k);
 #pragma unroll
                 for (int t = 0; t < kMsmZ; ++t) acc[t] = __ffma2_rn(wd, r[(k + t) & (kMsmZ - 1)], acc[t]);
             }
@@ -318,6 +326,27 @@ __global__ void __launch_bounds__(kMsmThreads) msm_conv_kernel(const __grid_cons
             out[(long long)(z0 + t) * zs] = acc[t].x;
             if (y1) out[(long long)(z0 + t) * zs + Lv.n[0]] = acc[t].y;
         }
+}
+
+__global__ void __launch_bounds__(kMsmThreads) msm_conv_kernel(const __grid_constant__ MsmParams p) {
+    int l = 0;
+    while (l + 2 < p.levels && (long long)blockIdx.x >= p.lv[l + 1].cta_begin) ++l;
+    const MsmLevelDev &Lv = p.lv[l];
+    const long long local = (long long)blockIdx.x - Lv.cta_begin;
+    const int s = (int)(local % Lv.split);
+    const long long col = (local / Lv.split) * kMsmThreads + threadIdx.x;
+    if (col >= Lv.cols) return;
+    switch (Lv.plane) {
+        case 1 << 10: msm_conv_tile<1 << 10>(p, Lv, s, col); break;
+        case 1 << 11: msm_conv_tile<1 << 11>(p, Lv, s, col); break;
+        case 1 << 12: msm_conv_tile<1 << 12>(p, Lv, s, col); break;
+        case 1 << 13: msm_conv_tile<1 << 13>(p, Lv, s, col); break;
+        case 1 << 14: msm_conv_tile<1 << 14>(p, Lv, s, col); break;
+        case 1 << 15: msm_conv_tile<1 << 15>(p, Lv, s, col); break;
+        case 1 << 16: msm_conv_tile<1 << 16>(p, Lv, s, col); break;
+        case 1 << 17: msm_conv_tile<1 << 17>(p, Lv, s, col); break;
+        default: msm_conv_tile<1 << 18>(p, Lv, s, col); break;
+    }
 }
 
 // Top level: e_i = sum_j gtop[|i - j|^2] q_j over all top nodes; one warp
@@ -337,10 +366,10 @@ __global__ void __launch_bounds__(kMsmThreads) msm_top_kernel(const __grid_const
         const int jy = rj % T.n[1], jz = rj / T.n[1];
         const int dy = iy - jy, dz = iz - jz;
         const int d2 = dy * dy + dz * dz;
-        const float *q = T.q + ((long long)(jz + p.R) * T.qd[1] + (jy + p.R)) * T.qd[0] + p.R;
+        const float2 *q = T.q + (long long)(jz + p.R) * T.plane + (long long)(jy + p.R) * T.qd[0] + p.R;
         for (int jx = 0; jx < T.n[0]; ++jx) {
             const int dx = ix - jx;
-            acc = fmaf(p.gtop[d2 + dx * dx], q[jx], acc);
+            acc = fmaf(p.gtop[d2 + dx * dx], q[jx].x, acc);
         }
     }
 #pragma unroll
@@ -508,16 +537,17 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_kernel(const __grid_co
 }
 
 // Interpolation for grid spacings h <= h0: one CTA per 8x8x8-point brick.
-// The brick's points need at most kSpan level-0 nodes per axis; those are
+// The brick's points need at most SPAN level-0 nodes per axis; those are
 // staged in shared memory and the tensor-product sum is done one axis at a
 // time (z, then y, then x), so a point costs about 12 FMAs instead of 64.
-constexpr int kInterpSpan = 12;
-
+// SPAN is a compile-time bound (6, 8 or 12) so that the staging loops index
+// with constant divisors.
+template <int SPAN>
 __global__ void __launch_bounds__(kMsmThreads) msm_interp_brick_kernel(const __grid_constant__ MsmParams p,
                                                                         const __grid_constant__ InterpParams g) {
-    __shared__ float E[kInterpSpan][kInterpSpan][kInterpSpan];  // [z][y][x] nodes around the brick
-    __shared__ float S1[kBrick][kInterpSpan][kInterpSpan];      // [point z][node y][node x]
-    __shared__ float S2[kBrick][kBrick][kInterpSpan];           // [point z][point y][node x]
+    __shared__ float E[SPAN][SPAN][SPAN];     // [z][y][x] nodes around the brick
+    __shared__ float S1[kBrick][SPAN][SPAN];  // [point z][node y][node x]
+    __shared__ float S2[kBrick][kBrick][SPAN];  // [point z][point y][node x]
     __shared__ float wgt[3][kBrick][4];
     __shared__ int off[3][kBrick];
     __shared__ int base[3], cnt[3];
@@ -528,8 +558,9 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_brick_kernel(const __g
     const int bx = blockIdx.x % nbx, by = (blockIdx.x / nbx) % nby, bz = blockIdx.x / (nbx * nby);
     const MsmLevelDev &L0 = p.lv[0];
     if (tid == 0) bad = 0;
+    __syncthreads();
     if (tid < 3 * kBrick) {
-        // per axis d and point p of the brick: node offset and the 4 weights
+        // per axis d and point pt of the brick: node offset and the 4 weights
         const int d = tid / kBrick, pt = tid % kBrick;
         const int n = d == 0 ? g.nx : (d == 1 ? g.ny : g.nz);
         const int b = d == 0 ? bx : (d == 1 ? by : bz);
@@ -537,46 +568,51 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_brick_kernel(const __g
         const int idx = min(kBrick * b + pt, n - 1);  // points past the edge repeat the last one
         const float t = msm_t(fmaf((float)idx, g.h, o), p.o[d], p.h0);
         const int k = min(max((int)floorf(t), 0), p.cells[d] - 1);
-        const int idx0 = kBrick * b;
-        const float t0 = msm_t(fmaf((float)idx0, g.h, o), p.o[d], p.h0);
+        const float t0 = msm_t(fmaf((float)(kBrick * b), g.h, o), p.o[d], p.h0);
         const int k0 = min(max((int)floorf(t0), 0), p.cells[d] - 1);
         off[d][pt] = k - k0;
         for (int a = 0; a < 4; ++a) wgt[d][pt][a] = msm_phi(t - (float)(k - 1 + a));
         if (pt == kBrick - 1) {
             base[d] = k0 - 1 - L0.lo[d];  // array index of the first node
             cnt[d] = k - k0 + 4;
-            if (k - k0 + 4 > kInterpSpan || k < k0) atomicOr(&bad, 1);
+            if (k - k0 + 4 > SPAN || k < k0) atomicOr(&bad, 1);
         }
     }
     __syncthreads();
-    if (bad) {  // cannot happen for h <= h0; recorded rather than trusted
+    if (bad) {  // the host picks SPAN from h/h0; recorded rather than trusted
         if (tid == 0) atomicOr(p.status, CP_DEVICE_RANGE);
         return;
     }
     const int cx = cnt[0], cy = cnt[1], cz = cnt[2];
-    for (int e = tid; e < cx * cy * cz; e += kMsmThreads) {
-        const int ex = e % cx, ey = (e / cx) % cy, ez = e / (cx * cy);
-        const int gx = base[0] + ex, gy = base[1] + ey, gz = base[2] + ez;
-        const bool in = gx >= 0 && gx < L0.n[0] && gy >= 0 && gy < L0.n[1] && gz >= 0 && gz < L0.n[2];
-        E[ez][ey][ex] = in ? L0.e[((long long)gz * L0.n[1] + gy) * L0.n[0] + gx] : 0.0f;
+    for (int e = tid; e < SPAN * SPAN * SPAN; e += kMsmThreads) {
+        const int ex = e % SPAN, ey = (e / SPAN) % SPAN, ez = e / (SPAN * SPAN);
+        if (ex < cx && ey < cy && ez < cz) {
+            const int gx = base[0] + ex, gy = base[1] + ey, gz = base[2] + ez;
+            const bool in = gx >= 0 && gx < L0.n[0] && gy >= 0 && gy < L0.n[1] && gz >= 0 && gz < L0.n[2];
+            E[ez][ey][ex] = in ? L0.e[((long long)gz * L0.n[1] + gy) * L0.n[0] + gx] : 0.0f;
+        }
     }
     __syncthreads();
-    for (int e = tid; e < kBrick * cy * cx; e += kMsmThreads) {  // along z
-        const int ex = e % cx, ey = (e / cx) % cy, pz = e / (cx * cy);
-        const int o = off[2][pz];
-        float v = 0.0f;
+    for (int e = tid; e < kBrick * SPAN * SPAN; e += kMsmThreads) {  // along z
+        const int ex = e % SPAN, ey = (e / SPAN) % SPAN, pz = e / (SPAN * SPAN);
+        if (ex < cx && ey < cy) {
+            const int o = off[2][pz];
+            float v = 0.0f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) v = fmaf(wgt[2][pz][c], E[o + c][ey][ex], v);
-        S1[pz][ey][ex] = v;
+            for (int c = 0; c < 4; ++c) v = fmaf(wgt[2][pz][c], E[o + c][ey][ex], v);
+            S1[pz][ey][ex] = v;
+        }
     }
     __syncthreads();
-    for (int e = tid; e < kBrick * kBrick * cx; e += kMsmThreads) {  // along y
-        const int ex = e % cx, py = (e / cx) % kBrick, pz = e / (cx * kBrick);
-        const int o = off[1][py];
-        float v = 0.0f;
+    for (int e = tid; e < kBrick * kBrick * SPAN; e += kMsmThreads) {  // along y
+        const int ex = e % SPAN, py = (e / SPAN) % kBrick, pz = e / (SPAN * kBrick);
+        if (ex < cx) {
+            const int o = off[1][py];
+            float v = 0.0f;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) v = fmaf(wgt[1][py][b], S1[pz][o + b][ex], v);
-        S2[pz][py][ex] = v;
+            for (int b = 0; b < 4; ++b) v = fmaf(wgt[1][py][b], S1[pz][o + b][ex], v);
+            S2[pz][py][ex] = v;
+        }
     }
     __syncthreads();
     // along x: thread -> 4 consecutive points of one brick row
@@ -748,10 +784,14 @@ int make_msm_geometry(int n_atoms, const Grid &g, cp_vec3 dlo, cp_vec3 dhi, floa
         L.q_dims[l][0] = (int)n0 + 2 * R;
         L.q_dims[l][1] = (int)(2 * ((n1 + 1) / 2)) + 2 * R;
         L.q_dims[l][2] = (int)(kMsmZ * ((n2 + kMsmZ - 1) / kMsmZ)) + 2 * R;
-        const long long qn = (long long)L.q_dims[l][0] * L.q_dims[l][1] * L.q_dims[l][2];
+        long long plane = kMsmMinPlane;
+        while (plane < (long long)L.q_dims[l][0] * L.q_dims[l][1]) plane *= 2;
+        if (plane > kMsmMaxPlane) return CP_ERR_TOO_LARGE;
+        L.q_plane[l] = (int)plane;
+        const long long qn = plane * L.q_dims[l][2];
         if (qn > INT_MAX) return CP_ERR_TOO_LARGE;
         L.off_q[l] = off;
-        off = align256(off + 4 * (size_t)qn);
+        off = align256(off + 8 * (size_t)qn);
         L.off_e[l] = off;
         off = align256(off + 4 * (size_t)(n0 * n1 * n2));
     }
@@ -853,7 +893,8 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
             v.n[d] = L.n[l][d];
             v.qd[d] = L.q_dims[l][d];
         }
-        v.q = reinterpret_cast<float *>(ws + L.off_q[l]);
+        v.q = reinterpret_cast<float2 *>(ws + L.off_q[l]);
+        v.plane = L.q_plane[l];
         v.e = reinterpret_cast<float *>(ws + L.off_e[l]);
         v.scale = (float)std::ldexp(1.0, -l);
         if (l + 1 < L.levels) {
@@ -912,8 +953,14 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     const unsigned iblocks = (unsigned)((ip.quads + kMsmThreads - 1) / kMsmThreads);
     const long long nbricks = (long long)((g.nx + kBrick - 1) / kBrick) * ((g.ny + kBrick - 1) / kBrick) *
                               ((g.nz + kBrick - 1) / kBrick);
-    if (g.h <= lattice_h && nbricks <= 0x7fffffffLL)
-        msm_interp_brick_kernel<<<(unsigned)nbricks, kMsmThreads, 0, st>>>(p, ip);
+    // nodes a brick's 8 points need per axis: at most ceil(7 h / h0) + 4
+    const int span = (int)std::ceil(7.0 * (double)g.h / (double)lattice_h + 1e-4) + 4;
+    if (g.h <= lattice_h && span <= 6 && nbricks <= 0x7fffffffLL)
+        msm_interp_brick_kernel<6><<<(unsigned)nbricks, kMsmThreads, 0, st>>>(p, ip);
+    else if (g.h <= lattice_h && span <= 8 && nbricks <= 0x7fffffffLL)
+        msm_interp_brick_kernel<8><<<(unsigned)nbricks, kMsmThreads, 0, st>>>(p, ip);
+    else if (g.h <= lattice_h && span <= 12 && nbricks <= 0x7fffffffLL)
+        msm_interp_brick_kernel<12><<<(unsigned)nbricks, kMsmThreads, 0, st>>>(p, ip);
     else if ((g.nx % 4 == 0) && aligned(V, 16))
         msm_interp_kernel<true><<<iblocks, kMsmThreads, 0, st>>>(p, ip);
     else

@@ -374,8 +374,11 @@ typedef struct {
     cp_vec3 lattice_origin;            /* o (fp32) */
     int q_dims[CP_MSM_MAX_LEVELS][3];  /* padded charge lattice: x + 2R, y rounded up to even + 2R,
                                         * z rounded up to a multiple of 8 + 2R */
-    size_t off_q[CP_MSM_MAX_LEVELS];   /* float32 [q_dims z][q_dims y][q_dims x]; node (i, j, k) of the
-                                        * level at [k - lo z + R][j - lo y + R][i - lo x + R], zero padding */
+    int q_plane[CP_MSM_MAX_LEVELS];    /* its z stride in entries: a power of two >= q_dims x * q_dims y */
+    size_t off_q[CP_MSM_MAX_LEVELS];   /* float32 pairs [q_dims z][q_plane]: entry (x, y, z) at
+                                        * z * q_plane + y * q_dims x + x holds (q(x, y, z), q(x, y+1, z));
+                                        * node (i, j, k) of the level is entry (i - lo x + R, j - lo y + R,
+                                        * k - lo z + R); zero padding */
     size_t off_e[CP_MSM_MAX_LEVELS];   /* lattice potentials, float32 [n z][n y][n x] */
     size_t off_cells;                  /* the cell sort's sections start here (a cp_cutoff_layout with
                                         * capacity 0, offsets relative to this one) */

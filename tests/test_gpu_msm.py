@@ -57,6 +57,9 @@ CASES = [
                                              margin=9.0, cutoff=3.0, bin_size=1.5), 0.5),
     ("coarse", workloads.random_case(703, 900, (30, 30, 30), h=0.5, origin=(0.0, 0.0, 0.0), margin=2.0,
                                      cutoff=5.0, bin_size=2.5), 2.5),
+    # grid spacing above the lattice spacing: the per-quad interpolation kernel
+    ("grid_coarser_than_lattice", workloads.random_case(706, 600, (21, 14, 11), h=1.0, origin=(0.5, -1.0, 2.0),
+                                                        margin=3.0, cutoff=3.0, bin_size=1.5), 0.7),
 ]
 
 
@@ -86,7 +89,12 @@ def test_lattice_stages_match_oracle():
         n = int(np.prod(dims))
         return ws[off: off + 4 * n].view(torch.float32).view(*dims[::-1]).cpu().numpy().astype(np.float64)
 
-    q0 = lattice(L.off_q[0], tuple(L.q_dims[0]))
+    qd, plane = tuple(L.q_dims[0]), int(L.q_plane[0])
+    pairs = ws[L.off_q[0]: L.off_q[0] + 8 * plane * qd[2]].view(torch.float32).view(qd[2], plane, 2)
+    pairs = pairs.cpu().numpy().astype(np.float64)
+    q0 = pairs[:, :qd[0] * qd[1], 0].reshape(qd[2], qd[1], qd[0])
+    second = pairs[:, :qd[0] * qd[1], 1].reshape(qd[2], qd[1], qd[0])
+    assert np.array_equal(second[:, :-1, :], q0[:, 1:, :]) and not second[:, -1, :].any()
     n0 = geo.levels[0].n
     inner = q0[R:R + n0[2], R:R + n0[1], R:R + n0[0]]
     ref_q0 = msm.anterpolate(w.atoms, geo)
