@@ -566,9 +566,12 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_brick_kernel(const __g
         const int b = d == 0 ? bx : (d == 1 ? by : bz);
         const float o = d == 0 ? g.ox : (d == 1 ? g.oy : g.oz);
         const int idx = min(kBrick * b + pt, n - 1);  // points past the edge repeat the last one
-        const float t = msm_t(fmaf((float)idx, g.h, o), p.o[d], p.h0);
+        // lattice coordinate of the point: weights only, so a reciprocal
+        // multiply suffices (the cell sort's exact division is for atoms)
+        const float inv_h0 = 1.0f / p.h0;
+        const float t = (fmaf((float)idx, g.h, o) - p.o[d]) * inv_h0;
         const int k = min(max((int)floorf(t), 0), p.cells[d] - 1);
-        const float t0 = msm_t(fmaf((float)(kBrick * b), g.h, o), p.o[d], p.h0);
+        const float t0 = (fmaf((float)(kBrick * b), g.h, o) - p.o[d]) * inv_h0;
         const int k0 = min(max((int)floorf(t0), 0), p.cells[d] - 1);
         off[d][pt] = k - k0;
         for (int a = 0; a < 4; ++a) wgt[d][pt][a] = msm_phi(t - (float)(k - 1 + a));
