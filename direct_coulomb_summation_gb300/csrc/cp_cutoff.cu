@@ -24,12 +24,13 @@
 //     more than the capacity.
 //   * Consumer warp w owns sub-box w of the brick (8 x 4 x 4 points; each
 //     lane 4 consecutive x points as two f32x2 pairs).  For every stage each
-//     consumer warp tests a quarter of the atoms against all four sub-boxes
-//     (distance to the box < c) and appends each atom to the list of every
-//     sub-box it can reach, in per-writer segments so that the order never
-//     depends on timing; after a consumer-only barrier each warp runs its
-//     own list through the pair loop, adding the switched term
-//     q * (rsqrt(r^2) - (GC0 + r^2 (GC1 + r^2 GC2))) for r^2 < c^2.
+//     consumer warp tests all the stage's atoms against its own sub-box
+//     (distance to the box < c), copies those that pass into its own list
+//     (stage order), releases the stage and runs the list through the pair
+//     loop, adding the switched term
+//     q * (rsqrt(r^2) - (GC0 + r^2 (GC1 + r^2 GC2))) for r^2 < c^2.  The
+//     consumer warps never wait for one another: each may run ahead of the
+//     others by up to the ring's depth.
 //   * Unused fixed slots sit at 1e18 A and never pass the sub-box test,
 //     which replaces the lecture's stop-at-the-first-empty-slot rule.
 #include <cuda_runtime.h>
@@ -338,24 +339,15 @@ __device__ __forceinline__ int brick_home_dev(int brick, int m, double h, double
 
 // Atoms per shared-memory stage.  The producer packs as many bin runs (or
 // pieces of runs) into a stage as fit, so a stage usually holds several
-// runs and the consumers synchronise once per stage, not once per run.
-// Each consumer warp sorts one 32-atom quarter of a stage into the lists.
-constexpr int kWarpSlots = 32;
-constexpr int kStageAtoms = kWarpSlots * kBrickConsumerWarps;
-
-// Barrier among the consumer warps only (the producer warp keeps streaming).
-__device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kBrickConsumerWarps) : "memory");
-}
+// runs; every consumer warp tests the whole stage against its own sub-box.
+constexpr int kStageAtoms = 128;
 
 template <int K, bool VEC, bool COUNT>
 __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __grid_constant__ BrickParams p) {
     __shared__ __align__(128) float4 ring[kBrickStages][kStageAtoms];
-    // list b (atoms that can reach sub-box b) in segments, one per writing
-    // warp, so that list order never depends on timing
-    __shared__ __align__(16) float4 wlist[kBrickConsumerWarps][kBrickConsumerWarps][kWarpSlots];
-    __shared__ int wcount[kBrickConsumerWarps][kBrickConsumerWarps];
-    __shared__ volatile int abort_flag;
+    // each consumer warp's list of the stage's atoms that can reach its
+    // sub-box, in stage order
+    __shared__ __align__(16) float4 wlist[kBrickConsumerWarps][kStageAtoms];
     __shared__ uint64_t full[kBrickStages], empty[kBrickStages];
     __shared__ volatile int stage_n[kBrickStages];
 
@@ -370,7 +362,6 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kBrickConsumerWarps);
         }
-        abort_flag = 0;
         mbar_init_fence();
     }
     __syncthreads();
@@ -503,87 +494,73 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
     const float z = fmaf((float)k, p.h, p.oz);
     const float2 NG0 = make_float2(-p.gc0, -p.gc0), NG1 = make_float2(-p.gc1, -p.gc1);
     const float2 NG2 = make_float2(-p.gc2, -p.gc2);
-    // the four sub-boxes share their x extent; two y and two z extents
+    // this warp's sub-box: all 8 x, 4 y rows, 4 z planes
     const float lox = fmaf((float)(kBrick * bx), p.h, p.ox), hix = fmaf((float)(kBrick * bx + 7), p.h, p.ox);
-    const float loy0 = fmaf((float)(kBrick * by), p.h, p.oy), hiy0 = fmaf((float)(kBrick * by + 3), p.h, p.oy);
-    const float loy1 = fmaf((float)(kBrick * by + 4), p.h, p.oy), hiy1 = fmaf((float)(kBrick * by + 7), p.h, p.oy);
-    const float loz0 = fmaf((float)(kBrick * bz), p.h, p.oz), hiz0 = fmaf((float)(kBrick * bz + 3), p.h, p.oz);
-    const float loz1 = fmaf((float)(kBrick * bz + 4), p.h, p.oz), hiz1 = fmaf((float)(kBrick * bz + 7), p.h, p.oz);
+    const int wy0 = kBrick * by + (warp & 1) * 4, wz0 = kBrick * bz + (warp >> 1) * 4;
+    const float loy = fmaf((float)wy0, p.h, p.oy), hiy = fmaf((float)(wy0 + 3), p.h, p.oy);
+    const float loz = fmaf((float)wz0, p.h, p.oz), hiz = fmaf((float)(wz0 + 3), p.h, p.oz);
     const unsigned below = (1u << lane) - 1u;
+    float4 *list = &wlist[warp][0];
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     unsigned long long n_real = 0, n_near = 0, n_useful = 0;  // COUNT only
     for (int seq = 0;; ++seq) {
         const int s = seq % kBrickStages;
         const bool got = mbar_wait(&full[s], (uint32_t)((seq / kBrickStages) & 1), p.status);
-        if (!got) abort_flag = 1;
         const int n = got ? stage_n[s] : -1;
-        if (n >= 0) {
-            // (1) this warp's quarter of the stage against all four sub-boxes;
-            // an atom that can reach sub-box b is appended to segment `warp`
-            // of list b
-            const int i = kWarpSlots * warp + lane;
+        if (n < 0) break;  // end of the stream (or a wait that ran out: recorded)
+        // (1) every atom of the stage against this warp's sub-box; those that
+        // can reach it are copied, in stage order, to the warp's own list
+        int cnt = 0;
+        for (int i0s = 0; i0s < n; i0s += 32) {
+            const int i = i0s + lane;
             const bool valid = i < n;
             const float4 a = valid ? ring[s][i] : make_float4(kPadCoord, kPadCoord, kPadCoord, 0.f);
-            if (COUNT && valid && a.x < 1.0e17f) ++n_real;
+            if (COUNT && warp == 0 && valid && a.x < 1.0e17f) ++n_real;
             const float ex = fmaxf(fmaxf(lox - a.x, a.x - hix), 0.0f);
-            const float ey0 = fmaxf(fmaxf(loy0 - a.y, a.y - hiy0), 0.0f);
-            const float ey1 = fmaxf(fmaxf(loy1 - a.y, a.y - hiy1), 0.0f);
-            const float ez0 = fmaxf(fmaxf(loz0 - a.z, a.z - hiz0), 0.0f);
-            const float ez1 = fmaxf(fmaxf(loz1 - a.z, a.z - hiz1), 0.0f);
-            const float e2y0 = fmaf(ey0, ey0, ex * ex), e2y1 = fmaf(ey1, ey1, ex * ex);
-#pragma unroll
-            for (int b = 0; b < kBrickConsumerWarps; ++b) {
-                const float ez = (b >> 1) ? ez1 : ez0;
-                const bool near = fmaf(ez, ez, (b & 1) ? e2y1 : e2y0) < p.cull2;
-                const unsigned m = __ballot_sync(0xffffffffu, near);
-                if (near) wlist[b][warp][__popc(m & below)] = a;
-                if (lane == 0) wcount[b][warp] = __popc(m);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+            const float ey = fmaxf(fmaxf(loy - a.y, a.y - hiy), 0.0f);
+            const float ez = fmaxf(fmaxf(loz - a.z, a.z - hiz), 0.0f);
+            const bool near = fmaf(ez, ez, fmaf(ey, ey, ex * ex)) < p.cull2;
+            const unsigned m = __ballot_sync(0xffffffffu, near);
+            if (near) list[cnt + __popc(m & below)] = a;
+            cnt += __popc(m);
         }
-        consumer_sync();  // every list segment of this stage is written
-        if (abort_flag || n < 0) break;
-        // (2) every atom listed for this warp's sub-box against the lane's 4 points
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled: the list holds copies
+        if (COUNT) n_near += (unsigned)cnt;
+        // (2) every listed atom against the lane's 4 points
         float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-        for (int g = 0; g < kBrickConsumerWarps; ++g) {
-            const int cnt = wcount[warp][g];
-            if (COUNT) n_near += (unsigned)cnt;
-            const float4 *list = &wlist[warp][g][0];
 #pragma unroll 2
-            for (int t = 0; t < cnt; ++t) {
-                const float4 a = list[t];  // broadcast
-                // differences as scalars (dy^2 + dz^2 is the same for the
-                // lane's 4 points), written into the f32x2 operand pairs
-                const float dy = y - a.y, dz = z - a.z;
-                const float d = fmaf(dy, dy, dz * dz);
-                const float2 dyz2 = make_float2(d, d);
-                const float2 dx01 = make_float2(x[0] - a.x, x[1] - a.x);
-                const float2 dx23 = make_float2(x[2] - a.x, x[3] - a.x);
-                const float2 r01 = __ffma2_rn(dx01, dx01, dyz2);
-                const float2 r23 = __ffma2_rn(dx23, dx23, dyz2);
-                // e = rsqrt(r^2) - g(r^2), with -g by Horner on the negated coefficients
-                const float2 rs01 = make_float2(sfu_rsqrt(r01.x), sfu_rsqrt(r01.y));
-                const float2 rs23 = make_float2(sfu_rsqrt(r23.x), sfu_rsqrt(r23.y));
-                const float2 e01 = __fadd2_rn(rs01, __ffma2_rn(__ffma2_rn(r01, NG2, NG1), r01, NG0));
-                const float2 e23 = __fadd2_rn(rs23, __ffma2_rn(__ffma2_rn(r23, NG2, NG1), r23, NG0));
-                if (r01.x < p.c2) part[0] = fmaf(a.w, e01.x, part[0]);
-                if (r01.y < p.c2) part[1] = fmaf(a.w, e01.y, part[1]);
-                if (r23.x < p.c2) part[2] = fmaf(a.w, e23.x, part[2]);
-                if (r23.y < p.c2) part[3] = fmaf(a.w, e23.y, part[3]);
-                if (COUNT) {
-                    const float r2c[4] = {r01.x, r01.y, r23.x, r23.y};
+        for (int t = 0; t < cnt; ++t) {
+            const float4 a = list[t];  // broadcast
+            // differences as scalars (dy^2 + dz^2 is the same for the
+            // lane's 4 points), written into the f32x2 operand pairs
+            const float dy = y - a.y, dz = z - a.z;
+            const float d = fmaf(dy, dy, dz * dz);
+            const float2 dyz2 = make_float2(d, d);
+            const float2 dx01 = make_float2(x[0] - a.x, x[1] - a.x);
+            const float2 dx23 = make_float2(x[2] - a.x, x[3] - a.x);
+            const float2 r01 = __ffma2_rn(dx01, dx01, dyz2);
+            const float2 r23 = __ffma2_rn(dx23, dx23, dyz2);
+            // e = rsqrt(r^2) - g(r^2), with -g by Horner on the negated coefficients
+            const float2 rs01 = make_float2(sfu_rsqrt(r01.x), sfu_rsqrt(r01.y));
+            const float2 rs23 = make_float2(sfu_rsqrt(r23.x), sfu_rsqrt(r23.y));
+            const float2 e01 = __fadd2_rn(rs01, __ffma2_rn(__ffma2_rn(r01, NG2, NG1), r01, NG0));
+            const float2 e23 = __fadd2_rn(rs23, __ffma2_rn(__ffma2_rn(r23, NG2, NG1), r23, NG0));
+            if (r01.x < p.c2) part[0] = fmaf(a.w, e01.x, part[0]);
+            if (r01.y < p.c2) part[1] = fmaf(a.w, e01.y, part[1]);
+            if (r23.x < p.c2) part[2] = fmaf(a.w, e23.x, part[2]);
+            if (r23.y < p.c2) part[3] = fmaf(a.w, e23.y, part[3]);
+            if (COUNT) {
+                const float r2c[4] = {r01.x, r01.y, r23.x, r23.y};
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (r2c[c] < p.c2 && i0 + c < p.nx && j < p.ny && k < p.nz) ++n_useful;
-                }
+                for (int c = 0; c < 4; ++c)
+                    if (r2c[c] < p.c2 && i0 + c < p.nx && j < p.ny && k < p.nz) ++n_useful;
             }
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[c] += part[c];
-        consumer_sync();  // the lists are rewritten by the next stage
+        __syncwarp();  // the list is rewritten by the next stage
     }
 
     if (COUNT) {
@@ -598,7 +575,8 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
         if (lane == 0) {
             atomicAdd(&p.counts[0], n_useful);
             atomicAdd(&p.counts[1], n_near * 128ull);
-            // each real atom a lane sorted was examined against all 512 points
+            // warp 0 counted every real atom of the stream once; each was
+            // examined against all 512 points
             atomicAdd(&p.counts[2], n_real * 128ull * kBrickConsumerWarps);
         }
         return;
