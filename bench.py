@@ -560,16 +560,20 @@ def run_ours(args):
             "bound": "alu",
             "kernel": "direct_kernel (cp_direct)",
             "achieved": achieved_direct,
-            "peak": peak_direct,
+            "peak": per_sm_split * sm_clk,
             "unit": "pair evals/s",
-            "frac": achieved_direct / peak_direct,
+            "frac": achieved_direct / (per_sm_split * sm_clk),
             "traffic": traffic,
-            "peak_basis": f"{n_sm} SMs x {per_sm_direct:.2f} pairs/clk/SM = min(SFU rsqrt {r_mufu:.2f}, "
-                          f"FFMA {r_ffma:.1f}/3, issue 128/4) measured per SM clock, x {f_mhz:.0f} MHz ({clock_basis})",
-            "peak_split_rsqrt": per_sm_split * sm_clk,
-            "frac_split_rsqrt": achieved_direct / (per_sm_split * sm_clk),
-            "split_basis": f"rsqrt shared between SFU and FMA pipe at the best share {f_split:.2f}: "
-                           f"{per_sm_split:.1f} pairs/clk/SM",
+            "peak_basis": f"{n_sm} SMs x {per_sm_split:.1f} pairs/clk/SM x {f_mhz:.0f} MHz ({clock_basis}): "
+                          f"the pair (1 rsqrt, 3 FP32 ops) with its rsqrt shared between the SFU ({r_mufu:.2f}/clk/SM "
+                          f"measured) and the FMA pipe (magic-constant estimate + two Newton steps, 7 FP32 ops; "
+                          f"FFMA {r_ffma:.1f} lanes/clk/SM measured) at the best share {f_split:.2f}, "
+                          f"(1 - f)/R_sfu = (3 + 7f)/R_fp32",
+            "peak_sfu_only": peak_direct,
+            "frac_sfu_only": achieved_direct / peak_direct,
+            "sfu_only_basis": f"{n_sm} SMs x {per_sm_direct:.2f} pairs/clk/SM = min(SFU rsqrt {r_mufu:.2f}, "
+                              f"FFMA {r_ffma:.1f}/3, issue 128/4): the scope table's bound for rsqrt on the SFU "
+                              f"alone, which the kernel exceeds by moving a share of the rsqrts to the FMA pipe",
         },
         "direct": {
             "pair_evals_per_s": direct_rate,

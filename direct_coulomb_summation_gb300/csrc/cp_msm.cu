@@ -73,6 +73,16 @@ __device__ __forceinline__ float msm_phi(float t) {
     return a <= 1.0f ? inner : (a <= 2.0f ? outer : 0.0f);
 }
 
+// phi(t) for |t| <= 2 (a node and an atom or point of one of the four cells
+// around it): one cubic in a = |t| whose coefficients are chosen by a <= 1,
+// 1 - 5a^2/2 + 3a^3/2 inside, 2 - 4a + 5a^2/2 - a^3/2 outside.
+__device__ __forceinline__ float msm_phi_near(float t) {
+    const float a = fabsf(t);
+    const bool in = a <= 1.0f;
+    const float c3 = in ? 1.5f : -0.5f, c2 = in ? -2.5f : 2.5f, c1 = in ? 0.0f : -4.0f, c0 = in ? 1.0f : 2.0f;
+    return fmaf(fmaf(fmaf(c3, a, c2), a, c1), a, c0);
+}
+
 // g_c(r) = gamma(r/c)/c in fp64 with explicit roundings (no contraction).
 __device__ double msm_g64(double r, double c) {
     const double s = __ddiv_rn(r, c);
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(kMsmThreads) msm_anterp_kernel(const __grid_co
                     const int b = p.cell_start[row + cx0], e = p.cell_start[row + cx1 + 1];
                     for (int t = b; t < e; ++t) {
                         const float4 a = p.cell_t[t];
-                        acc = fmaf(a.w, msm_phi(a.x - fi) * msm_phi(a.y - fj) * msm_phi(a.z - fk), acc);
+                        acc = fmaf(a.w, msm_phi_near(a.x - fi) * msm_phi_near(a.y - fj) * msm_phi_near(a.z - fk), acc);
                     }
                 }
         }

@@ -42,3 +42,34 @@ def test_graph_capture_and_replay():
     assert torch.equal(Vd, 2.0 * ref_d)
     assert torch.allclose(Vc, 2.0 * ref_c, rtol=0, atol=0)
     assert cp.device_status() == 0
+
+
+def test_graph_capture_of_the_multilevel_map():
+    """cutoff + cp_msm_longrange (accumulating) in one graph: the replay gives
+    the eager multilevel map, bit for bit."""
+    w = workloads.random_case(72, 2500, (36, 20, 16), margin=3.0, cutoff=4.0, bin_size=2.0)
+    h0 = 1.0
+    a = to_dev(w.atoms)
+    dom = cp.atom_bounds(a)
+    V = torch.empty((16, 20, 36), device="cuda")
+    need_c = cp.cutoff_workspace_bytes(w.n_atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, 0)
+    need_m = cp.msm_workspace_bytes(w.n_atoms, w.shape, w.origin, w.h, w.cutoff, h0, dom)
+    ws_c = torch.empty(need_c, dtype=torch.uint8, device="cuda")
+    ws_m = torch.empty(need_m, dtype=torch.uint8, device="cuda")
+
+    def run(out):
+        cp.cutoff(a, w.shape, w.origin, w.h, w.cutoff, w.bin_size, 0, workspace=ws_c, out=out)
+        cp.msm_longrange(a, w.shape, w.origin, w.h, w.cutoff, h0, domain=dom, accumulate=True, workspace=ws_m,
+                         out=out)
+
+    ref = torch.empty_like(V)
+    run(ref)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run(V)
+    V.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(V, ref)
+    assert cp.device_status() == 0
