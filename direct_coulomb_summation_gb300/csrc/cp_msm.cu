@@ -55,6 +55,7 @@ constexpr int kMsmZ = 8;                                      // nodes a lattice
 constexpr long long kMsmTargetThreads = 1LL << 17;            // lattice-cutoff threads worth splitting for
 constexpr int kMsmMaxSplit = 64;
 constexpr int kMsmThreads = 128;
+constexpr int kReduceGroup = 8;  // lanes per node in the partial-sum reduction of heavily split levels
 constexpr long long kMsmMinPlane = 1024;     // z-plane strides of the charge lattices: powers of two
 constexpr long long kMsmMaxPlane = 1 << 18;  // in this range, each a compile-time constant of the stencil loop
 
@@ -180,39 +181,36 @@ __global__ void __launch_bounds__(kMsmThreads) msm_tcoord_kernel(const __grid_co
     p.cell_t[t] = make_float4(msm_t(a.x, p.o[0], p.h0), msm_t(a.y, p.o[1], p.h0), msm_t(a.z, p.o[2], p.h0), a.w);
 }
 
-// q0 at every padded level-0 entry: zero in the padding, else the sum over
+// q0 at every level-0 node (the padding was zeroed before): the sum over
 // the atoms of the cells i-2 .. i+1 (per axis) of q Phi(t - i), in cell
-// order.
+// order.  One thread per node, nodes x fastest.
 __global__ void __launch_bounds__(kMsmThreads) msm_anterp_kernel(const __grid_constant__ MsmParams p) {
     const MsmLevelDev &L0 = p.lv[0];
-    const long long total = (long long)L0.qd[0] * L0.qd[1] * L0.qd[2];
+    const long long total = (long long)L0.n[0] * L0.n[1] * L0.n[2];
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx == 0 && p.cell_stats[1] != 0) atomicOr(p.status, CP_DEVICE_ATOMS_OUTSIDE);  // dropped by the sort
     if (idx >= total) return;
-    const int px = (int)(idx % L0.qd[0]);
-    const int py = (int)((idx / L0.qd[0]) % L0.qd[1]);
-    const int pz = (int)(idx / ((long long)L0.qd[0] * L0.qd[1]));
-    const int ax = px - p.R, ay = py - p.R, az = pz - p.R;  // array index within the level
+    const int ax = (int)(idx % L0.n[0]);
+    const int ay = (int)((idx / L0.n[0]) % L0.n[1]);
+    const int az = (int)(idx / ((long long)L0.n[0] * L0.n[1]));
+    const int i = ax + L0.lo[0], j = ay + L0.lo[1], k = az + L0.lo[2];  // node index
+    const float fi = (float)i, fj = (float)j, fk = (float)k;
+    const int cx0 = max(i - 2, 0), cx1 = min(i + 1, p.cells[0] - 1);
+    const int cy0 = max(j - 2, 0), cy1 = min(j + 1, p.cells[1] - 1);
+    const int cz0 = max(k - 2, 0), cz1 = min(k + 1, p.cells[2] - 1);
     float acc = 0.0f;
-    if (ax >= 0 && ax < L0.n[0] && ay >= 0 && ay < L0.n[1] && az >= 0 && az < L0.n[2]) {
-        const int i = ax + L0.lo[0], j = ay + L0.lo[1], k = az + L0.lo[2];  // node index
-        const float fi = (float)i, fj = (float)j, fk = (float)k;
-        const int cx0 = max(i - 2, 0), cx1 = min(i + 1, p.cells[0] - 1);
-        const int cy0 = max(j - 2, 0), cy1 = min(j + 1, p.cells[1] - 1);
-        const int cz0 = max(k - 2, 0), cz1 = min(k + 1, p.cells[2] - 1);
-        if (cx0 <= cx1) {
-            for (int cz = cz0; cz <= cz1; ++cz)
-                for (int cy = cy0; cy <= cy1; ++cy) {
-                    const long long row = ((long long)cz * p.cells[1] + cy) * p.cells[0];
-                    const int b = p.cell_start[row + cx0], e = p.cell_start[row + cx1 + 1];
-                    for (int t = b; t < e; ++t) {
-                        const float4 a = p.cell_t[t];
-                        acc = fmaf(a.w, msm_phi_near(a.x - fi) * msm_phi_near(a.y - fj) * msm_phi_near(a.z - fk), acc);
-                    }
+    if (cx0 <= cx1) {
+        for (int cz = cz0; cz <= cz1; ++cz)
+            for (int cy = cy0; cy <= cy1; ++cy) {
+                const long long row = ((long long)cz * p.cells[1] + cy) * p.cells[0];
+                const int b = p.cell_start[row + cx0], e = p.cell_start[row + cx1 + 1];
+                for (int t = b; t < e; ++t) {
+                    const float4 a = p.cell_t[t];
+                    acc = fmaf(a.w, msm_phi_near(a.x - fi) * msm_phi_near(a.y - fj) * msm_phi_near(a.z - fk), acc);
                 }
-        }
+            }
     }
-    msm_store_pair(L0, px, py, pz, acc);
+    msm_store_pair(L0, ax + p.R, ay + p.R, az + p.R, acc);
 }
 
 // Restriction weights phi(k/2) for fine offsets k = -3 .. 3 (k = +-2 weigh 0).
@@ -412,11 +410,20 @@ __global__ void __launch_bounds__(kMsmThreads) msm_reduce_prolong_kernel(const _
     const MsmLevelDev &F = p.lv[l];
     const MsmLevelDev &C = p.lv[l + 1];
     const long long nodes = (long long)F.n[0] * F.n[1] * F.n[2];
-    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= nodes) return;
+    // G consecutive lanes share a node when the split is large: lane g adds
+    // partials g, g + G, ... and the G sums meet by a fixed shuffle tree
+    const int G = F.split >= 16 ? kReduceGroup : 1;
+    const long long gidx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long idx = gidx / G;
+    const int g = (int)(gidx % G);
     float s = 0.0f;
-#pragma unroll 8
-    for (int k = 0; k < F.split; ++k) s += F.part[(long long)k * nodes + idx];
+    if (idx < nodes)
+        for (int k = g; k < F.split; k += G) s += F.part[(long long)k * nodes + idx];
+    if (G > 1) {
+#pragma unroll
+        for (int o = kReduceGroup / 2; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o, kReduceGroup);
+    }
+    if (idx >= nodes || g != 0) return;
     const int ax = (int)(idx % F.n[0]);
     const int ay = (int)((idx / F.n[0]) % F.n[1]);
     const int az = (int)(idx / ((long long)F.n[0] * F.n[1]));
@@ -924,7 +931,9 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     const long long nst = (long long)side * side * side + kMsmTopTable;
     msm_stencil_kernel<<<(unsigned)std::min<long long>((nst + 255) / 256, 1024), 256, 0, st>>>(p);
     const MsmLevelDev &L0 = p.lv[0];
-    const long long q0n = (long long)L0.qd[0] * L0.qd[1] * L0.qd[2];
+    const long long q0n = (long long)L0.n[0] * L0.n[1] * L0.n[2];
+    // the charge lattice's padding must be zero: clear it all, nodes follow
+    if (cudaMemsetAsync(L0.q, 0, (size_t)8 * L0.plane * L0.qd[2], st) != cudaSuccess) return CP_ERR_CUDA;
     if (n_atoms > 0) {
         msm_tcoord_kernel<<<(unsigned)((n_atoms + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p);
         ++launches;
@@ -947,7 +956,7 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     ++launches;
     for (int l = L.levels - 2; l >= 0; --l) {
         const MsmLevelDev &F = p.lv[l];
-        const long long fn = (long long)F.n[0] * F.n[1] * F.n[2];
+        const long long fn = (long long)F.n[0] * F.n[1] * F.n[2] * (F.split >= 16 ? kReduceGroup : 1);
         msm_reduce_prolong_kernel<<<(unsigned)((fn + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p, l);
         ++launches;
     }
