@@ -101,11 +101,17 @@ SIGNATURES = {
     "cp_msm_workspace_bytes": (_SZ, [_I, *_GRID, cp_vec3, cp_vec3, _F, _F]),
     "cp_msm_longrange": (_I, [_P, _I, *_GRID, cp_vec3, cp_vec3, _F, _F, _P, _SZ, _P, _I, _P]),
     "cp_atom_bounds": (_I, [_P, _I, _P, _P]),
+    "cp_probe_wait_timeout": (_I, [ctypes.c_ulonglong, _P, _P]),
 }
 
 
+def checked() -> bool:
+    """True when CPMAP_CHECKED=1 selects the bounds-checked build."""
+    return os.environ.get("CPMAP_CHECKED", "") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.LIB_CHECKED if checked() else _build.LIB
 
 
 def load(auto_build: bool = True):
@@ -114,11 +120,12 @@ def load(auto_build: bool = True):
     with _LOCK:
         if _LIB is not None:
             return _LIB
-        if not _build.up_to_date():
+        if not _build.up_to_date(checked()):
             if not auto_build:
-                raise RuntimeError("libcpmap.so is missing or stale; run direct_coulomb_summation_gb300.build")
-            _build.build()
-        lib = ctypes.CDLL(_build.LIB)
+                raise RuntimeError(f"{os.path.basename(library_path())} is missing or stale; "
+                                   "run direct_coulomb_summation_gb300.build")
+            _build.build(checked=checked())
+        lib = ctypes.CDLL(library_path())
         for name, (res, args) in SIGNATURES.items():
             fn = getattr(lib, name)
             fn.restype = res

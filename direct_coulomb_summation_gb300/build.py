@@ -1,10 +1,16 @@
 """Builds libcpmap.so (the sm_103a CUDA library behind the C ABI) in-tree.
 
-    python -m direct_coulomb_summation_gb300.build
+    python -m direct_coulomb_summation_gb300.build [--checked]
 
 Each .cu file is compiled to an object in parallel with nvcc for
 ``sm_103a`` only, then linked into ``_build/libcpmap.so``.  A stamp of the
 sources and flags decides whether a rebuild is needed.
+
+``checked=True`` builds ``_build/libcpmap_checked.so`` from the same sources
+with -DCP_BOUNDS_CHECKS: every runtime-computed index of the kernels'
+global and shared-memory accesses is tested, and a violation records
+CP_DEVICE_RANGE in the device status word and skips the access.  Setting
+CPMAP_CHECKED=1 makes the binding load that library.
 """
 from __future__ import annotations
 
@@ -22,6 +28,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libcpmap.so")
 STAMP = os.path.join(BUILD, "libcpmap.stamp")
+LIB_CHECKED = os.path.join(BUILD, "libcpmap_checked.so")
+STAMP_CHECKED = os.path.join(BUILD, "libcpmap_checked.stamp")
+CHECKED_FLAGS = ["-DCP_BOUNDS_CHECKS"]
 
 SOURCES = ["cp_host.cu", "cp_direct.cu", "cp_cutoff.cu", "cp_msm.cu", "cp_probe.cu", "cp_variants.cu"]
 HEADERS = ["cp_device.cuh", "cp_internal.h"]
@@ -57,15 +66,22 @@ def _digest(extra=()) -> str:
     return h.hexdigest()
 
 
-def up_to_date() -> bool:
-    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
+def _paths(checked: bool):
+    if checked:
+        return LIB_CHECKED, STAMP_CHECKED, os.path.join(BUILD, "obj_checked"), CHECKED_FLAGS
+    return LIB, STAMP, os.path.join(BUILD, "obj"), []
+
+
+def up_to_date(checked: bool = False) -> bool:
+    lib, stamp, _, extra = _paths(checked)
+    if not (os.path.exists(lib) and os.path.exists(stamp)):
         return False
-    with open(STAMP) as f:
-        return f.read().strip() == _digest()
+    with open(stamp) as f:
+        return f.read().strip() == _digest(extra)
 
 
-def _compile(nvcc: str, src: str, obj: str, verbose: bool) -> str:
-    cmd = [nvcc, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+def _compile(nvcc: str, src: str, obj: str, verbose: bool, extra=()) -> str:
+    cmd = [nvcc, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -74,34 +90,43 @@ def _compile(nvcc: str, src: str, obj: str, verbose: bool) -> str:
     return res.stdout + res.stderr
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if needed) and return the path of libcpmap.so."""
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile (if needed) and return the path of libcpmap.so (or of the
+    checked build, libcpmap_checked.so)."""
+    lib, stamp, objdir, extra = _paths(checked)
+    if not force and up_to_date(checked):
+        return lib
     nvcc = nvcc_path()
-    objdir = os.path.join(BUILD, "obj")
     os.makedirs(objdir, exist_ok=True)
     jobs = []
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as pool:
         for name in SOURCES:
             src = os.path.join(CSRC, name)
             obj = os.path.join(objdir, name.replace(".cu", ".o"))
-            jobs.append((name, pool.submit(_compile, nvcc, src, obj, verbose)))
+            jobs.append((name, pool.submit(_compile, nvcc, src, obj, verbose, extra)))
         logs = [(name, fut.result()) for name, fut in jobs]
     if verbose:
         for name, log in logs:
             if log.strip():
                 print(f"--- {name}\n{log}", file=sys.stderr)
     objs = [os.path.join(objdir, n.replace(".cu", ".o")) for n in SOURCES]
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     res = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
-        f.write(_digest())
-    return LIB
+    os.replace(tmp, lib)
+    with open(stamp, "w") as f:
+        f.write(_digest(extra))
+    return lib
+
+
+def build_all(force: bool = False) -> tuple:
+    """Both libraries, compiled concurrently: (release path, checked path)."""
+    with cf.ThreadPoolExecutor(max_workers=2) as pool:
+        rel = pool.submit(build, force, False, False)
+        chk = pool.submit(build, force, False, True)
+        return rel.result(), chk.result()
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

@@ -66,6 +66,7 @@ struct BinParams {
     int2 *bin_rank;
     int *block_sums;
     int *block_prefix;
+    unsigned int *status;  // checked build: index checks record here
 };
 
 // fp32 bin coordinate: floor(float(float(a - bo) / b)), -1 outside [0, nb)
@@ -91,7 +92,7 @@ __global__ void bin_count_kernel(const __grid_constant__ BinParams p) {
     const int uy = bin_axis(a.y, p.bo[1], p.b, p.nb[1]);
     const int uz = bin_axis(a.z, p.bo[2], p.b, p.nb[2]);
     int bin = -1, rank = 0;
-    if (ux >= 0 && uy >= 0 && uz >= 0) {
+    if (ux >= 0 && uy >= 0 && uz >= 0 && CP_IN((uz * p.nb[1] + uy) * p.nb[0] + ux, p.nbins, p.status)) {
         bin = (uz * p.nb[1] + uy) * p.nb[0] + ux;
         rank = atomicAdd(&p.count[bin], 1);
     } else {
@@ -180,7 +181,7 @@ __global__ void bin_scatter_kernel(const __grid_constant__ BinParams p) {
     const int2 br = p.bin_rank[i];
     if (br.x < 0) return;
     const int pos = p.start[br.x] + p.block_prefix[br.x / kScanBlock] + br.y;
-    p.csr_index[pos] = i;
+    if (CP_IN(pos, p.n, p.status)) p.csr_index[pos] = i;
 }
 
 // One warp per bin: rank the bin's input indices by comparison, write the
@@ -195,9 +196,11 @@ __global__ void __launch_bounds__(256) bin_sort_pack_kernel(const __grid_constan
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int bin = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (bin < p.nbins) {
-        const int n = p.count[bin];
-        const int s = p.start[bin] + p.block_prefix[bin / kScanBlock];
+    const int nb_ = bin < p.nbins ? p.count[bin] : 0;
+    const int sb_ = bin < p.nbins ? p.start[bin] + p.block_prefix[bin / kScanBlock] : 0;
+    if (bin < p.nbins && (nb_ == 0 || (CP_IN(sb_, p.n, p.status) && CP_IN(sb_ + nb_ - 1, p.n, p.status)))) {
+        const int n = nb_;
+        const int s = sb_;
         int *tmp = reinterpret_cast<int *>(p.bin_rank);  // free after the scatter
         for (int c0 = 0; c0 < n; c0 += 32) {
             const int e = (c0 + lane < n) ? p.csr_index[s + c0 + lane] : INT_MAX;
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(256) bin_sort_pack_kernel(const __grid_constan
                 const int m = min(32, n - c1);
                 for (int k = 0; k < m; ++k) rank += (__shfl_sync(0xffffffffu, f, k) < e) ? 1 : 0;
             }
-            if (c0 + lane < n) {
+            if (c0 + lane < n && CP_IN(e, p.n, p.status)) {
                 const float4 a = p.atoms[e];
                 tmp[s + rank] = e;
                 p.csr_atoms[s + rank] = a;
@@ -248,9 +251,12 @@ __global__ void __launch_bounds__(256) bin_sort_pack_lane_kernel(const __grid_co
     const int lane = threadIdx.x & 31;
     const int bin0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * 32;
     const int bin = bin0 + lane;
-    const bool valid = bin < p.nbins;
-    const int n = valid ? p.count[bin] : 0;
-    const int s = valid ? p.start[bin] + p.block_prefix[bin / kScanBlock] : 0;
+    const int n0_ = bin < p.nbins ? p.count[bin] : 0;
+    const int s0_ = bin < p.nbins ? p.start[bin] + p.block_prefix[bin / kScanBlock] : 0;
+    const bool valid =
+        bin < p.nbins && (n0_ == 0 || (CP_IN(s0_, p.n, p.status) && CP_IN(s0_ + n0_ - 1, p.n, p.status)));
+    const int n = valid ? n0_ : 0;
+    const int s = valid ? s0_ : 0;
     int *tmp = reinterpret_cast<int *>(p.bin_rank);  // free after the scatter
     const bool small = n <= kLaneSortMax;
     if (valid && small) {
@@ -258,6 +264,7 @@ __global__ void __launch_bounds__(256) bin_sort_pack_lane_kernel(const __grid_co
             const int e = p.csr_index[s + c0];
             int rank = 0;
             for (int c1 = 0; c1 < n; ++c1) rank += (p.csr_index[s + c1] < e) ? 1 : 0;
+            if (!CP_IN(e, p.n, p.status)) continue;
             const float4 a = p.atoms[e];
             tmp[s + rank] = e;
             p.csr_atoms[s + rank] = a;
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(256) bin_sort_pack_lane_kernel(const __grid_co
                 const int m = min(32, bn - c1);
                 for (int k = 0; k < m; ++k) rank += (__shfl_sync(0xffffffffu, f, k) < e) ? 1 : 0;
             }
-            if (c0 + lane < bn) {
+            if (c0 + lane < bn && CP_IN(e, p.n, p.status)) {
                 const float4 a = p.atoms[e];
                 tmp[bs + rank] = e;
                 p.csr_atoms[bs + rank] = a;
@@ -327,6 +334,8 @@ struct BrickParams {
     const float4 *csr_atoms;
     float *V;
     unsigned int *status;
+    int n_csr;             // atoms in the bin-sorted array (checked build)
+    long long n_padded;    // fixed slots in all bins (checked build)
     unsigned long long *counts;  // pair-counting variant only: [3] see cp_cutoff_pair_counts
     int n_runs;
     int runs[kMaxRuns];  // packed int8 (dy, dz, dx_lo, dx_hi)
@@ -432,7 +441,8 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
                 for (int t = 0; t < nr; ++t) {
                     const int l = __shfl_sync(0xffffffffu, lo, t);
                     const int h = __shfl_sync(0xffffffffu, hi, t);
-                    if (lane == 0 && h > l) push(p.csr_atoms + l, h - l);
+                    if (lane == 0 && h > l && CP_IN(l, p.n_csr, p.status) && CP_IN(h - 1, p.n_csr, p.status))
+                        push(p.csr_atoms + l, h - l);
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
             }
@@ -451,7 +461,9 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
                             const unsigned nz = __ballot_sync(0xffffffffu, cnt > 0);
                             if (nz != 0u && lane == 0) {
                                 const int l0 = __ffs(nz) - 1, l1 = 31 - __clz(nz);
-                                push(p.padded + (long long)(f32 + l0) * K, (l1 - l0 + 1) * K);
+                                if (CP_IN((long long)(f32 + l0) * K, p.n_padded, p.status) &&
+                                    CP_IN((long long)(f32 + l1 + 1) * K - 1, p.n_padded, p.status))
+                                    push(p.padded + (long long)(f32 + l0) * K, (l1 - l0 + 1) * K);
                             }
                         } else {
                             const int st = lane < nb32 ? p.start[f32 + lane] : 0;
@@ -461,7 +473,8 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
                                 ov &= ov - 1u;
                                 const int cj = __shfl_sync(0xffffffffu, cnt, jb);
                                 const int sj = __shfl_sync(0xffffffffu, st, jb);
-                                if (lane == 0) push(p.csr_atoms + sj + K, cj - K);
+                                if (lane == 0 && CP_IN(sj + K, p.n_csr, p.status) && CP_IN(sj + cj - 1, p.n_csr, p.status))
+                                    push(p.csr_atoms + sj + K, cj - K);
                             }
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -522,7 +535,7 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
             const float ez = fmaxf(fmaxf(loz - a.z, a.z - hiz), 0.0f);
             const bool near = fmaf(ez, ez, fmaf(ey, ey, ex * ex)) < p.cull2;
             const unsigned m = __ballot_sync(0xffffffffu, near);
-            if (near) list[cnt + __popc(m & below)] = a;
+            if (near && CP_IN(cnt + __popc(m & below), kStageAtoms, p.status)) list[cnt + __popc(m & below)] = a;
             cnt += __popc(m);
         }
         __syncwarp();
@@ -583,8 +596,10 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
     }
     if (j < p.ny && k < p.nz) {
         float *row = p.V + ((long long)k * p.ny + j) * p.nx;
+        const long long total = (long long)p.nx * p.ny * p.nz, at = ((long long)k * p.ny + j) * p.nx + i0;
         if (VEC) {
-            if (i0 < p.nx) *reinterpret_cast<float4 *>(row + i0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            if (i0 < p.nx && CP_IN(at + 3, total, p.status))
+                *reinterpret_cast<float4 *>(row + i0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -625,6 +640,7 @@ BinParams bin_params(const float4 *atoms, int n_atoms, const BinGeom &bg, const 
     b.block_sums = reinterpret_cast<int *>(ws + off);
     off += (4 * nblk + 255) & ~(size_t)255;
     b.block_prefix = reinterpret_cast<int *>(ws + off);
+    b.status = device_status_ptr();
     return b;
 }
 
@@ -705,6 +721,8 @@ int launch_bricks_k(const Prepared &P, const OffsetList &L, float *V, cudaStream
     p.count = P.bp.count;
     p.start = P.bp.start;
     p.csr_atoms = P.bp.csr_atoms;
+    p.n_csr = P.bp.n;
+    p.n_padded = (long long)P.bg.nbins * P.bp.K;
     p.V = V;
     p.counts = counts;
     p.status = device_status_ptr();

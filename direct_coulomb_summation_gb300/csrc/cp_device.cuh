@@ -11,6 +11,21 @@ namespace cpmap {
 // CP_DEVICE_WAIT_TIMEOUT and carries on (nanoseconds of %globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// Index checks of the checked build (compiled with -DCP_BOUNDS_CHECKS):
+// CP_IN(i, n, status) is true when 0 <= i < n; when it is not, the checked
+// build records CP_DEVICE_RANGE (0x2) in *status and the caller skips the
+// access.  In the release build every check is the constant `true`.
+#ifdef CP_BOUNDS_CHECKS
+__device__ __forceinline__ bool cp_in_range(long long i, long long n, unsigned int *status) {
+    if (i >= 0 && i < n) return true;
+    atomicOr(status, 0x2u);
+    return false;
+}
+#define CP_IN(i, n, status) (::cpmap::cp_in_range((long long)(i), (long long)(n), (status)))
+#else
+#define CP_IN(i, n, status) true
+#endif
+
 // rsqrt on the SFU (MUFU): one instruction, flush-to-zero variant.
 __device__ __forceinline__ float sfu_rsqrt(float x) {
     float y;
@@ -87,16 +102,21 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 // time-out it sets CP_DEVICE_WAIT_TIMEOUT in *status and returns false; the
 // caller then carries on (its data are wrong, the status says so) so that no
 // thread is left behind at a later block barrier.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *status) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, unsigned int *status,
+                                                unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(status, 1u /* CP_DEVICE_WAIT_TIMEOUT */);
             return false;
         }
     }
     return true;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *status) {
+    return mbar_wait_limit(bar, parity, status, kWaitLimitNs);
 }
 
 // 1-D bulk copy global -> this CTA's shared memory, completion counted on

@@ -77,8 +77,11 @@ struct DirectParams {
 template <bool VEC>
 __device__ __forceinline__ void store_quad(const DirectParams &p, int i0, int y, int z, float4 v) {
     if (y >= p.ny || z >= p.nz) return;
+    const long long at = ((long long)z * p.ny + y) * p.nx + i0;
+    if (!CP_IN(at, (long long)p.nx * p.ny * p.nz, p.status)) return;
     float *row = p.V + ((long long)z * p.ny + y) * p.nx;
     if (VEC) {
+        if (!CP_IN(at + 3, (long long)p.nx * p.ny * p.nz, p.status)) return;
         *reinterpret_cast<float4 *>(row + i0) = v;
     } else {
         if (i0 + 0 < p.nx) row[i0 + 0] = v.x;
@@ -137,8 +140,13 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
     auto issue = [&](int tl, int stage) {
         const int n = min(kDirectTile, n_local - tl * kDirectTile);
         const uint32_t bytes = (uint32_t)n * 16u;
-        mbar_arrive_expect_tx(&full[stage], bytes);
-        bulk_g2s(ring + stage * kDirectTile, p.atoms + a_begin + (long long)tl * kDirectTile, bytes, &full[stage]);
+        const long long first = a_begin + (long long)tl * kDirectTile;
+        if (CP_IN(first, p.n_atoms, p.status) && CP_IN(first + n - 1, p.n_atoms, p.status)) {
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            bulk_g2s(ring + stage * kDirectTile, p.atoms + first, bytes, &full[stage]);
+        } else {
+            mbar_arrive(&full[stage]);  // checked build only: no copy, the status says so
+        }
     };
     if (tid == 0) {
         for (int s = 0; s < kDirectStages && s < n_tiles; ++s) issue(s, s);

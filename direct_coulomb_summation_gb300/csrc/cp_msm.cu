@@ -125,6 +125,7 @@ struct MsmParams {
     const float4 *cell_atoms;
     float4 *cell_t;  // per cell-sorted atom: lattice coordinates (t x, t y, t z) and q
     long long ncells;
+    int n_atoms;
     const int *cell_stats;
     unsigned int *status;
     double h0_64, a64, lim2;
@@ -134,7 +135,12 @@ struct MsmParams {
 // Writes charge q of padded entry (x, y, z): as the first half of its own
 // pair and the second half of the pair of (x, y-1, z); the last row's
 // second halves (beyond the lattice) are zero.
-__device__ __forceinline__ void msm_store_pair(const MsmLevelDev &L, int x, int y, int z, float q) {
+__device__ __forceinline__ void msm_store_pair(const MsmLevelDev &L, int x, int y, int z, float q,
+                                               unsigned int *status) {
+    const long long at = (long long)z * L.plane + (long long)y * L.qd[0] + x;
+    if (!CP_IN(at, (long long)L.plane * L.qd[2], status) ||
+        (y > 0 && !CP_IN(at - L.qd[0], (long long)L.plane * L.qd[2], status)))
+        return;
     float2 *base = L.q + (long long)z * L.plane + x;
     float *own = reinterpret_cast<float *>(base + (long long)y * L.qd[0]);
     own[0] = q;
@@ -204,13 +210,14 @@ __global__ void __launch_bounds__(kMsmThreads) msm_anterp_kernel(const __grid_co
             for (int cy = cy0; cy <= cy1; ++cy) {
                 const long long row = ((long long)cz * p.cells[1] + cy) * p.cells[0];
                 const int b = p.cell_start[row + cx0], e = p.cell_start[row + cx1 + 1];
+                if (e > b && !(CP_IN(b, p.n_atoms, p.status) && CP_IN(e - 1, p.n_atoms, p.status))) continue;
                 for (int t = b; t < e; ++t) {
                     const float4 a = p.cell_t[t];
                     acc = fmaf(a.w, msm_phi_near(a.x - fi) * msm_phi_near(a.y - fj) * msm_phi_near(a.z - fk), acc);
                 }
             }
     }
-    msm_store_pair(L0, ax + p.R, ay + p.R, az + p.R, acc);
+    msm_store_pair(L0, ax + p.R, ay + p.R, az + p.R, acc, p.status);
 }
 
 // Restriction weights phi(k/2) for fine offsets k = -3 .. 3 (k = +-2 weigh 0).
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(kMsmThreads) msm_restrict_kernel(const __grid_
             acc = fmaf(msm_rw(kOff[c]), sz, acc);
         }
     }
-    msm_store_pair(C, px, py, pz, acc);
+    msm_store_pair(C, px, py, pz, acc, p.status);
 }
 
 // Lattice cutoff of every level below the top.  CTA -> (level, tile,
@@ -296,6 +303,10 @@ __device__ __forceinline__ void msm_conv_tile(const MsmParams &p, const MsmLevel
         // w[m] = (W, W) at dz = m - hw
         const float2 *q = base + dy * pitch + dx - hw * PLANE;
         const float2 *w = p.W + c * side + R - hw;
+        if (!CP_IN(q - Lv.q, (long long)PLANE * Lv.qd[2], p.status) ||
+            !CP_IN(q - Lv.q + (long long)(taps + kMsmZ - 2) * PLANE, (long long)PLANE * Lv.qd[2], p.status) ||
+            !CP_IN(w - p.W + taps - 1, (long long)side * side * side, p.status))
+            continue;
         // ring of 8 pairs: slot j holds the window node m' = j (mod 8), so
         // no register moves are needed
         float2 r[kMsmZ];
@@ -328,6 +339,7 @@ __device__ __forceinline__ void msm_conv_tile(const MsmParams &p, const MsmLevel
     const long long zs = (long long)Lv.n[0] * Lv.n[1];
     float *out = Lv.part + (long long)s * nodes + (long long)y0 * Lv.n[0] + x;
     const bool y1 = y0 + 1 < Lv.n[1];
+    if (!CP_IN(s, Lv.split, p.status)) return;
 #pragma unroll
     for (int t = 0; t < kMsmZ; ++t)
         if (z0 + t < Lv.n[2]) {
@@ -375,9 +387,10 @@ __global__ void __launch_bounds__(kMsmThreads) msm_top_kernel(const __grid_const
         const int dy = iy - jy, dz = iz - jz;
         const int d2 = dy * dy + dz * dz;
         const float2 *q = T.q + (long long)(jz + p.R) * T.plane + (long long)(jy + p.R) * T.qd[0] + p.R;
+        if (!CP_IN(q - T.q + T.n[0] - 1, (long long)T.plane * T.qd[2], p.status)) continue;
         for (int jx = 0; jx < T.n[0]; ++jx) {
             const int dx = ix - jx;
-            acc = fmaf(p.gtop[d2 + dx * dx], q[jx].x, acc);
+            if (CP_IN(d2 + dx * dx, kMsmTopTable, p.status)) acc = fmaf(p.gtop[d2 + dx * dx], q[jx].x, acc);
         }
     }
 #pragma unroll
@@ -649,6 +662,7 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_brick_kernel(const __g
     }
     const int i0 = kBrick * bx + 4 * half, j = kBrick * by + py, k = kBrick * bz + pz;
     if (j >= g.ny || k >= g.nz) return;
+    if (!CP_IN(((long long)k * g.ny + j) * g.nx + i0, (long long)g.nx * g.ny * g.nz, p.status)) return;
     float *row = g.V + ((long long)k * g.ny + j) * g.nx;
     if (i0 + 3 < g.nx && (g.nx % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.V) & 15) == 0)) {
         float4 *dst = reinterpret_cast<float4 *>(row + i0);
@@ -899,6 +913,7 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     p.cell_stats = reinterpret_cast<const int *>(cells_ws + geo.sortL.off_stats);
     p.cell_t = reinterpret_cast<float4 *>(ws + geo.off_tcoord);
     p.ncells = geo.cells.nbins;
+    p.n_atoms = n_atoms;
     p.status = device_status_ptr();
     if (!p.status) return CP_ERR_CUDA;
     p.h0_64 = geo.h0;

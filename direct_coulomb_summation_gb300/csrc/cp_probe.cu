@@ -73,6 +73,17 @@ __global__ void eval_rsqrt_kernel(const float *x, float *y, int n) {
     if (i + 1 < n) y[i + 1] = r.y;
 }
 
+// One thread waits on a shared-memory barrier that nothing arrives at, with
+// the kernels' bounded wait cut to limit_ns: the wait gives up, records
+// CP_DEVICE_WAIT_TIMEOUT and the kernel returns.
+__global__ void wait_timeout_kernel(unsigned long long limit_ns, unsigned int *status, int *gave_up) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+    *gave_up = mbar_wait_limit(&bar, 0, status, limit_ns) ? 0 : 1;
+}
+
 }  // namespace cpmap
 
 using namespace cpmap;
@@ -142,6 +153,17 @@ CP_API int cp_probe_pipe_rate(int kind, int warps, int iters, double *ops_per_cl
     cudaFree(cycles);
     cudaFree(sink);
     return rc;
+}
+
+CP_API int cp_probe_wait_timeout(unsigned long long limit_ns, int *gave_up, void *stream) {
+    if (!gave_up || limit_ns == 0 || limit_ns > kWaitLimitNs) return CP_ERR_INVALID_ARGUMENT;
+    if (!aligned(gave_up, 4)) return CP_ERR_MISALIGNED;
+    unsigned int *status = device_status_ptr();
+    if (!status) return CP_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, status, gave_up);
+    if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
+    note_launches(1);
+    return CP_OK;
 }
 
 }  // extern "C"

@@ -453,6 +453,15 @@ CP_API int cp_eval_rsqrt(int kind, const float *x, float *y, int n, void *stream
  * Returns CP_OK, CP_ERR_INVALID_ARGUMENT or CP_ERR_CUDA. */
 CP_API int cp_probe_pipe_rate(int kind, int warps, int iters, double *ops_per_clk, double *ms, void *stream);
 
+/* Failure-path check of the kernels' bounded waits (no page counterpart):
+ * one thread waits on a shared-memory barrier that nothing arrives at, with
+ * the wait limit cut to limit_ns (1 .. 2e9 ns); the wait gives up, sets
+ * CP_DEVICE_WAIT_TIMEOUT in the device status word and the kernel returns,
+ * writing 1 to the DEVICE int *gave_up (4-byte aligned).  Asynchronous on
+ * `stream`; the GPU context stays usable.  Returns CP_OK,
+ * CP_ERR_INVALID_ARGUMENT, CP_ERR_MISALIGNED or CP_ERR_CUDA. */
+CP_API int cp_probe_wait_timeout(unsigned long long limit_ns, int *gave_up, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

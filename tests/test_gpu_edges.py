@@ -70,3 +70,25 @@ def test_concurrent_streams():
         assert_within_bound(d.cpu().numpy(), ref, bound, "direct")
         ref, bound = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, cc)
         assert_within_bound(c.cpu().numpy(), ref, bound, "cutoff")
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """A wait on a barrier that nothing arrives at runs out after its limit
+    (1 ms here), records CP_DEVICE_WAIT_TIMEOUT and returns; the context stays
+    usable and the status word is clean again once read."""
+    lib = cp.library()
+    assert cp.device_status() == 0
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.cp_probe_wait_timeout(1_000_000, flag.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert flag.item() == 1
+    assert cp.device_status() & 0x1  # CP_DEVICE_WAIT_TIMEOUT
+    assert cp.device_status() == 0  # read and cleared
+    # the context still works
+    w = workloads.random_case(77, 50, (8, 8, 4))
+    V = cp.direct(torch.from_numpy(w.atoms).cuda(), w.shape, w.origin, w.h)
+    torch.cuda.synchronize()
+    assert torch.isfinite(V).all()
+    assert lib.cp_probe_wait_timeout(0, flag.data_ptr(), None) == -1
+    assert lib.cp_probe_wait_timeout(3_000_000_000, flag.data_ptr(), None) == -1
