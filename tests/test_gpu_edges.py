@@ -92,3 +92,50 @@ def test_bounded_wait_gives_up_and_reports():
     assert torch.isfinite(V).all()
     assert lib.cp_probe_wait_timeout(0, flag.data_ptr(), None) == -1
     assert lib.cp_probe_wait_timeout(3_000_000_000, flag.data_ptr(), None) == -1
+
+
+def test_maximum_grid():
+    """The largest grid the library takes, nx*ny*nz just below 2^31
+    (2048 x 1024 x 1023 points, an 8.6 GB V): direct, cutoff and long-range
+    maps with a few atoms, checked against the oracle at sampled points that
+    include the first and the very last grid point."""
+    shape, origin, h = (2048, 1024, 1023), (0.0, 0.0, 0.0), 0.5
+    assert shape[0] * shape[1] * shape[2] < 2 ** 31
+    rng = np.random.default_rng(4242)
+    lo = np.array([0.0, 0.0, 0.0])
+    hi = np.array([(shape[0] - 1) * h, (shape[1] - 1) * h, (shape[2] - 1) * h])
+    cells = rng.integers(0, (hi / h).astype(int), size=(6, 3))
+    pos = (cells + rng.uniform(0.1, 0.9, size=(6, 3))) * h
+    atoms = np.concatenate([pos, rng.uniform(-1.0, 1.0, size=(6, 1))], axis=1).astype(np.float32)
+    atoms[0, :3] = np.float32([1.3, 1.1, 0.7])      # near the first point
+    atoms[1, :3] = (hi - 0.3).astype(np.float32)    # near the last point
+    a = to_dev(atoms)
+    pts = np.concatenate([workloads.sample_points(shape, 300, seed=4243),
+                          np.array([[0, 0, 0], [shape[0] - 1, shape[1] - 1, shape[2] - 1],
+                                    [shape[0] - 1, 0, shape[2] - 1]])])
+    idx = torch.from_numpy(flat_index(shape, pts)).cuda()
+    V = torch.empty((shape[2], shape[1], shape[0]), dtype=torch.float32, device="cuda")
+    flat = V.view(-1)
+
+    cp.direct(a, shape, origin, h, out=V)
+    got = flat[idx].cpu().numpy()
+    ref, bound = oracle.direct(atoms, shape, origin, h, points=pts)
+    assert_within_bound(got, ref, bound, "direct, maximum grid")
+
+    c, b = 8.0, 16.0
+    cp.cutoff(a, shape, origin, h, c, b, 0, out=V)
+    got = flat[idx].cpu().numpy()
+    refc, boundc = oracle.cutoff_brute(atoms, shape, origin, h, c, points=pts)
+    assert np.all(np.abs(got - refc) <= 2e-4 * boundc + 1e-30)
+
+    from oracle import msm
+    dom = cp.atom_bounds(a)
+    cp.msm_longrange(a, shape, origin, h, c, 4.0, domain=dom, out=V)
+    got = flat[idx].cpu().numpy()
+    refl = msm.long_range(atoms, shape, origin, h, dom[0], dom[1], c, 4.0, points=pts)
+    bl = msm.abs_charge_bound(atoms, shape, origin, h, c, points=pts)
+    assert np.all(np.abs(got - refl) <= 1e-5 * bl)
+    torch.cuda.synchronize()
+    assert cp.device_status() == 0
+    del V, flat
+    torch.cuda.empty_cache()
