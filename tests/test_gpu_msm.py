@@ -191,3 +191,22 @@ def test_atom_bounds_exact():
     lo, hi = cp.atom_bounds(a)
     assert lo == tuple(float(v) for v in w.atoms[:, :3].min(0))
     assert hi == tuple(float(v) for v in w.atoms[:, :3].max(0))
+
+
+def test_large_clustered_workload_sampled():
+    """400^3 map, 800k atoms (30 % in Gaussian clusters), c = 12, h0 = 4 (four
+    levels from 57x58x59 nodes): 256 sampled points against the oracle's
+    multilevel sum, within 1e-5 of sum |q|/r (a looser scale than B(x),
+    from the C oracle, which is fast at this size)."""
+    w = workloads.make("cutoff_large")
+    h0 = 4.0
+    a = torch.from_numpy(w.atoms).cuda()
+    dom = cp.atom_bounds(a)
+    V = cp.msm_longrange(a, w.shape, w.origin, w.h, w.cutoff, h0, domain=dom)
+    torch.cuda.synchronize()
+    assert cp.device_status() == 0
+    pts = workloads.sample_points(w.shape, 256, seed=7002)
+    got = V.cpu().numpy().reshape(-1).astype(np.float64)[flat_index(w.shape, pts)]
+    ref = msm.long_range(w.atoms, w.shape, w.origin, w.h, dom[0], dom[1], w.cutoff, h0, points=pts)
+    _, scale = oracle.direct(w.atoms, w.shape, w.origin, w.h, points=pts)
+    _check(got, ref, scale, 1e-5, "large clustered long range")
