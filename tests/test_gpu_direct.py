@@ -35,7 +35,7 @@ def test_direct_small_full_grid(seed, n, shape, h, origin):
 
 
 @pytest.mark.parametrize("variant", sorted(cp.DIRECT_VARIANTS))
-@pytest.mark.parametrize("split", [1, 2, 3, 5, 8, 16])
+@pytest.mark.parametrize("split", [1, 2, 3, 5, 8, 11, 15, 16])
 def test_direct_every_variant_and_split(variant, split):
     w = workloads.random_case(200 + variant, 1537, (44, 13, 6), h=0.5, origin=(-1.0, 0.0, 2.0), margin=1.0)
     _check_full(w, variant=variant, split=split)

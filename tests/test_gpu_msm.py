@@ -210,3 +210,24 @@ def test_large_clustered_workload_sampled():
     ref = msm.long_range(w.atoms, w.shape, w.origin, w.h, dom[0], dom[1], w.cutoff, h0, points=pts)
     _, scale = oracle.direct(w.atoms, w.shape, w.origin, w.h, points=pts)
     _check(got, ref, scale, 1e-5, "large clustered long range")
+
+
+def test_public_api_with_host_arrays():
+    """numpy atoms in, host V out (pinned copies through the library): the
+    same maps as with device tensors, for the long-range part and for the
+    multilevel map."""
+    name, w, h0 = CASES[0]
+    dom = _domain(w.atoms)
+    host_long = cp.msm_longrange(w.atoms, w.shape, w.origin, w.h, w.cutoff, h0, domain=dom)
+    host_map = cp.msm_map(w.atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, h0, capacity=16, domain=dom)
+    assert not host_long.is_cuda and not host_map.is_cuda
+    a = torch.from_numpy(w.atoms).cuda()
+    dev_long = cp.msm_longrange(a, w.shape, w.origin, w.h, w.cutoff, h0, domain=dom)
+    dev_map = cp.msm_map(a, w.shape, w.origin, w.h, w.cutoff, w.bin_size, h0, capacity=16, domain=dom)
+    torch.cuda.synchronize()
+    assert torch.equal(host_long, dev_long.cpu())
+    assert torch.equal(host_map, dev_map.cpu())
+    # without a domain the binding asks the library for the atoms' bounding box
+    auto = cp.msm_longrange(a, w.shape, w.origin, w.h, w.cutoff, h0)
+    torch.cuda.synchronize()
+    assert torch.equal(auto, dev_long)
