@@ -39,6 +39,19 @@ __global__ void probe_kernel(int iters, float seed, long long *cycles, float *si
                 v[c] = y;
             }
         }
+        if (KIND == 4) {  // half the chains in f32x2 pairs, half scalar, interleaved
+#pragma unroll
+            for (int c = 0; c < kProbeChains / 2; c += 2) {
+                unsigned long long a, r;
+                asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(v[c]), "f"(v[c + 1]));
+                const unsigned long long m = 0x3f7fbe773f7fbe77ull;  // (0.999f, 0.999f)
+                const unsigned long long d = 0x3aaa64c33aaa64c3ull;  // (0.0013f, 0.0013f)
+                asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(m), "l"(d));
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(v[c]), "=f"(v[c + 1]) : "l"(r));
+                v[kProbeChains / 2 + c] = fmaf(v[kProbeChains / 2 + c], 0.999f, 0.0013f);
+                v[kProbeChains / 2 + c + 1] = fmaf(v[kProbeChains / 2 + c + 1], 0.999f, 0.0013f);
+            }
+        }
         if (KIND == 3) {
 #pragma unroll
             for (int c = 0; c < kProbeChains; c += 2) {
@@ -106,7 +119,7 @@ CP_API int cp_eval_rsqrt(int kind, const float *x, float *y, int n, void *stream
 }
 
 CP_API int cp_probe_pipe_rate(int kind, int warps, int iters, double *ops_per_clk, double *ms, void *stream) {
-    if (kind < 0 || kind > 3 || warps < 1 || warps > 32 || iters < 1 || !ops_per_clk) return CP_ERR_INVALID_ARGUMENT;
+    if (kind < 0 || kind > 4 || warps < 1 || warps > 32 || iters < 1 || !ops_per_clk) return CP_ERR_INVALID_ARGUMENT;
     DeviceInfo dev;
     int rc = device_info(&dev);
     if (rc) return rc;
@@ -118,8 +131,8 @@ CP_API int cp_probe_pipe_rate(int kind, int warps, int iters, double *ops_per_cl
         cudaFree(cycles);
         return CP_ERR_CUDA;
     }
-    void (*fns[4])(int, float, long long *, float *) = {probe_kernel<0>, probe_kernel<1>, probe_kernel<2>,
-                                                         probe_kernel<3>};
+    void (*fns[5])(int, float, long long *, float *) = {probe_kernel<0>, probe_kernel<1>, probe_kernel<2>,
+                                                         probe_kernel<3>, probe_kernel<4>};
     auto fn = fns[kind];
     rc = CP_OK;
     cudaEvent_t e0 = nullptr, e1 = nullptr;

@@ -447,7 +447,8 @@ CP_API int cp_eval_rsqrt(int kind, const float *x, float *y, int n, void *stream
 /* Microbenchmark of one SM pipe: every SM runs `warps` warps, each thread
  * issuing `iters` x 8 independent dependent-chain operations of kind
  * `kind` (0 = MUFU rsqrt.approx.ftz.f32, 1 = FP32 FFMA, 2 = MUFU ex2.approx,
- * 3 = FP32 FFMA in f32x2 pairs).  Writes the measured throughput in
+ * 3 = FP32 FFMA in f32x2 pairs, 4 = half the chains as f32x2 pairs and half
+ * as scalar FFMA, interleaved).  Writes the measured throughput in
  * operations per SM clock cycle (per-SM clock64 cycles, averaged over the
  * SMs) to *ops_per_clk and the kernel time to *ms.  Synchronous.
  * Returns CP_OK, CP_ERR_INVALID_ARGUMENT or CP_ERR_CUDA. */
