@@ -26,6 +26,7 @@ def _run(w, c, b, K=16, **kw):
     (303, 2500, (33, 9, 12), 0.5, (1.0, -4.0, 0.5), 4.0, 4.0),     # ragged bricks, big bins
     (304, 700, (16, 16, 1), 0.5, (0.0, 0.0, 5.0), 2.0, 0.75),      # single plane
     (305, 3000, (21, 9, 30), 0.3, (10.0, -5.0, 0.25), 1.9, 0.55),
+    (306, 1200, (14, 11, 9), 1.5, (0.5, 0.0, -1.0), 2.0, 0.8),      # grid spacing above the bin size
 ])
 def test_cutoff_small_full_grid(K, seed, n, shape, h, origin, c, b):
     w = workloads.random_case(seed, n, shape, h=h, origin=origin, margin=c + 1.0)

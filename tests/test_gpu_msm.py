@@ -57,6 +57,9 @@ CASES = [
                                              margin=9.0, cutoff=3.0, bin_size=1.5), 0.5),
     ("coarse", workloads.random_case(703, 900, (30, 30, 30), h=0.5, origin=(0.0, 0.0, 0.0), margin=2.0,
                                      cutoff=5.0, bin_size=2.5), 2.5),
+    # the largest stencil the library takes: R = ceil(2c/h0) = 24
+    ("max_radius", workloads.random_case(707, 300, (16, 14, 12), h=0.5, origin=(0.0, 0.0, 0.0), margin=2.0,
+                                         cutoff=6.0, bin_size=3.0), 0.5),
     # grid spacing above the lattice spacing: the per-quad interpolation kernel
     ("grid_coarser_than_lattice", workloads.random_case(706, 600, (21, 14, 11), h=1.0, origin=(0.5, -1.0, 2.0),
                                                         margin=3.0, cutoff=3.0, bin_size=1.5), 0.7),
