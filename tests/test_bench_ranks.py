@@ -60,3 +60,16 @@ def test_reference_arm_quiet_on_other_ranks():
                            "--warmup", "3"], capture_output=True, text=True, env=env, timeout=120)
     assert proc.returncode == 0
     assert proc.stdout.strip() == ""
+
+
+def test_clock_samples_that_invalidate_a_run():
+    import bench
+
+    ok = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert not bench.clocks_rejected(ok)
+    assert not bench.clocks_rejected(dict(ok, reasons=["sw_power_cap"]))  # kept and noted
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.clocks_rejected(dict(ok, reasons=[r]))
+    assert bench.clocks_rejected(dict(ok, sm_mhz=1200.0))  # stuck low with no reason: a clock lock
+    assert not bench.clocks_rejected(dict(ok, sm_mhz=1200.0, reasons=["sw_power_cap"]))
+    assert not bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]})
