@@ -122,3 +122,37 @@ def test_cutoff_large_workload_sampled():
     ref, bound = oracle.cutoff_binned(w.atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, points=pts)
     got = V.reshape(-1)[torch.from_numpy(flat_index(w.shape, pts)).cuda()].cpu().numpy()
     assert_within_bound(got, ref, bound, w.name)
+
+
+def _pairs_within(w, c, rel):
+    """Pairs (grid point, atom) with r^2 < c^2 (1 + rel), in fp64 from the same fp32 inputs."""
+    a = w.atoms[:, :3].astype(np.float64)
+    o = np.asarray([np.float32(v) for v in w.origin], dtype=np.float64)
+    h = float(np.float32(w.h))
+    ijk = workloads.grid_points(w.shape).astype(np.float64)
+    lim = float(np.float32(c)) ** 2 * (1.0 + rel)
+    total = 0
+    for s in range(0, ijk.shape[0], 2048):
+        g = o + ijk[s:s + 2048] * h
+        d2 = ((g[:, None, :] - a[None, :, :]) ** 2).sum(-1)
+        total += int(np.count_nonzero(d2 < lim))
+    return total
+
+
+@pytest.mark.parametrize("K", [0, 16])
+@pytest.mark.parametrize("seed,n,shape,h,origin,c,b", [
+    (321, 1500, (24, 20, 17), 0.5, (0.0, 0.0, 0.0), 6.0, 2.0),
+    (322, 1200, (19, 23, 16), 0.4, (-2.1, 0.7, 3.3), 3.0, 1.3),
+    (323, 2000, (33, 9, 12), 0.5, (1.0, -4.0, 0.5), 12.0, 4.0),   # the benchmark's c and bin size
+])
+def test_cutoff_useful_pairs_exact(K, seed, n, shape, h, origin, c, b):
+    """The counting variant of the brick traversal (behind the useful-pair rate the
+    benchmark reports) counts the pairs whose fp32 r^2 is below c^2 at stored
+    points.  That count must fall between the fp64 counts with c^2 narrowed and
+    widened by 2e-6 (the fp32 rounding of r^2 and of the grid coordinates), and
+    the traversal's evaluated and examined counts must bound it."""
+    w = workloads.random_case(seed, n, shape, h=h, origin=origin, margin=c + 1.0)
+    counts = cp.cutoff_pair_counts(to_dev(w.atoms), w.shape, w.origin, w.h, c, b, capacity=K)
+    lo, hi = _pairs_within(w, c, -2e-6), _pairs_within(w, c, 2e-6)
+    assert lo <= counts["useful"] <= hi, (counts, lo, hi)
+    assert counts["useful"] <= counts["evaluated"] <= counts["examined"]
