@@ -54,10 +54,16 @@ __all__ = [
     "msm_map",
 ]
 
-# index -> (PY, PZ, EMU): per-thread patch of 4 x-points times PY rows times PZ
-# planes; the first EMU of its 2*PY*PZ point pairs take rsqrt on the FMA pipe
-DIRECT_VARIANTS = {0: (4, 2, 0), 1: (2, 2, 0), 2: (4, 1, 0), 3: (2, 1, 0), 4: (1, 1, 0),
-                   5: (4, 2, 4), 6: (4, 2, 5), 7: (2, 2, 2), 8: (4, 1, 2), 9: (2, 1, 1)}
+# index -> (PX, PY, PZ, EMU, LS): a patch of PX x-points times PY rows times
+# PZ planes, the first EMU of its (PX/2)*PY*PZ point pairs with rsqrt on the
+# FMA pipe, shared by LS lanes that take every LS-th atom each.  The 2-point
+# (10, 11) and shared-patch (12-18) shapes serve grids too small to fill the
+# GPU with 4-point patches.
+DIRECT_VARIANTS = {0: (4, 4, 2, 0, 1), 1: (4, 2, 2, 0, 1), 2: (4, 4, 1, 0, 1), 3: (4, 2, 1, 0, 1),
+                   4: (4, 1, 1, 0, 1), 5: (4, 4, 2, 4, 1), 6: (4, 4, 2, 5, 1), 7: (4, 2, 2, 2, 1),
+                   8: (4, 4, 1, 2, 1), 9: (4, 2, 1, 1, 1), 10: (2, 1, 1, 0, 1), 11: (2, 2, 1, 0, 1),
+                   12: (4, 1, 1, 0, 4), 13: (4, 1, 1, 0, 2), 14: (4, 2, 1, 1, 4), 15: (4, 2, 1, 1, 2),
+                   16: (4, 2, 1, 1, 8), 17: (4, 2, 2, 2, 4), 18: (4, 4, 1, 2, 4)}
 
 
 class CpError(RuntimeError):

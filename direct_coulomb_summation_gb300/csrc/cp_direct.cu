@@ -5,20 +5,21 @@
 //   * gather: a thread owns grid points and every atom streams past it, so
 //     each thread writes only its own points and no atomics are needed
 //     (section 18.2);
-//   * coarsening: a thread owns a patch of 4 consecutive x points (one
-//     float4 of the x-fastest output) times PY rows in y times PZ planes in z;
+//   * coarsening: a thread owns a patch of PX = 4 (or, for grids too small
+//     to fill the GPU otherwise, 2) consecutive x points (one float4 or
+//     float2 of the x-fastest output) times PY rows in y times PZ planes in z;
 //     per atom the x differences are computed once per patch column and
 //     dy^2 + dz^2 once per row, so a pair costs FFMA (r^2), MUFU (rsqrt) and
 //     FFMA (accumulate) (section 18.3; the pwwt.cn article's section 三 does
 //     the same with 8 points per thread);
-//   * coalescing: neighbouring lanes own neighbouring x quads, so a warp
-//     stores 32 consecutive float4s of a row (section 18.4 and the article's
+//   * coalescing: neighbouring lanes own neighbouring x groups, so a warp
+//     stores 32 consecutive float4s (float2s) of a row (section 18.4 and the article's
 //     coarsen-plus-coalesce kernel, section 三);
 //   * atom tiles: instead of 4K-atom chunks in constant memory re-launched
 //     per chunk (section 18.2), one launch streams 256-atom tiles from global
 //     memory into a 3-stage shared-memory ring with 1-D TMA bulk copies; all
 //     threads read the same atom (a shared-memory broadcast);
-//   * f32x2: a thread's 4 x points are two register pairs, so r^2, the
+//   * f32x2: a thread's x points are register pairs, so r^2, the
 //     accumulate and the FMA-pipe rsqrt are paired Blackwell instructions;
 //   * rsqrt on two pipes: a compile-time share of each thread's point pairs
 //     takes its rsqrt on the FMA pipe (fma_rsqrt2) and the rest on the SFU,
@@ -37,6 +38,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "cp_device.cuh"
 #include "cp_internal.h"
@@ -52,8 +54,8 @@ constexpr int kDirectStages = 3;
 // totals (up to 16 point pairs of 8 bytes)
 constexpr int kDirectRingBytes = kDirectStages * kDirectTile * 16;
 constexpr int kDirectMaxPairs = 16;
-constexpr int direct_smem_bytes(int py, int pz) {
-    return kDirectRingBytes + kDirectThreads * (2 * py * pz) * 8;
+constexpr int direct_smem_bytes(int px, int py, int pz) {
+    return kDirectRingBytes + kDirectThreads * (px / 2 * py * pz) * 8;
 }
 constexpr int kMaxSplit = 16;       // cluster sizes above 8 are non-portable
 constexpr int kPortableSplit = 8;
@@ -64,7 +66,7 @@ struct DirectParams {
     int split;  // CTAs per cluster sharing one tile of points
     int nx, ny, nz;
     float ox, oy, oz, h;
-    int qx;         // x quads per row
+    int qx;         // x groups of PX points per row
     int yb;         // y blocks of PY rows
     long long npatch;
     float *V;
@@ -72,31 +74,44 @@ struct DirectParams {
 };
 
 
-// Stores one x quad of row (y, z): a float4 when the row is 16-byte aligned
-// and complete, else the in-range scalars.
-template <bool VEC>
-__device__ __forceinline__ void store_quad(const DirectParams &p, int i0, int y, int z, float4 v) {
+// Stores the PX x points from i0 of row (y, z): one float4 (PX = 4) or
+// float2 (PX = 2) when the row is aligned and the group complete, else the
+// in-range scalars.  v holds the points in x order (.z, .w unused for PX = 2).
+template <int PX, bool VEC>
+__device__ __forceinline__ void store_group(const DirectParams &p, int i0, int y, int z, float4 v) {
     if (y >= p.ny || z >= p.nz) return;
     const long long at = ((long long)z * p.ny + y) * p.nx + i0;
     if (!CP_IN(at, (long long)p.nx * p.ny * p.nz, p.status)) return;
     float *row = p.V + ((long long)z * p.ny + y) * p.nx;
     if (VEC) {
-        if (!CP_IN(at + 3, (long long)p.nx * p.ny * p.nz, p.status)) return;
-        *reinterpret_cast<float4 *>(row + i0) = v;
+        if (!CP_IN(at + PX - 1, (long long)p.nx * p.ny * p.nz, p.status)) return;
+        if (PX == 4)
+            *reinterpret_cast<float4 *>(row + i0) = v;
+        else
+            *reinterpret_cast<float2 *>(row + i0) = make_float2(v.x, v.y);
     } else {
         if (i0 + 0 < p.nx) row[i0 + 0] = v.x;
         if (i0 + 1 < p.nx) row[i0 + 1] = v.y;
-        if (i0 + 2 < p.nx) row[i0 + 2] = v.z;
-        if (i0 + 3 < p.nx) row[i0 + 3] = v.w;
+        if (PX == 4) {
+            if (i0 + 2 < p.nx) row[i0 + 2] = v.z;
+            if (i0 + 3 < p.nx) row[i0 + 3] = v.w;
+        }
     }
 }
 
-// A thread owns 4 x points (two f32x2 pairs) x PY rows x PZ planes, i.e.
-// 2*PY*PZ point pairs.  The first EMU pairs take their rsqrt on the FMA pipe
-// (fma_rsqrt2), the others on the SFU, so that both units share the work.
-template <int PY, int PZ, int EMU, bool VEC>
+// A patch is PX x points (PX/2 f32x2 pairs) x PY rows x PZ planes, i.e.
+// (PX/2)*PY*PZ point pairs.  The first EMU pairs take their rsqrt on the FMA
+// pipe (fma_rsqrt2), the others on the SFU, so that both units share the work.
+// LS neighbouring lanes share a patch, each taking every LS-th atom of a tile
+// (more warps for grids with few patches); their sums meet by a fixed
+// xor-shuffle tree, so every lane of the group holds the same total.
+template <int PX, int PY, int PZ, int EMU, int LS, bool VEC>
 __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_constant__ DirectParams p) {
-    constexpr int NP = 2 * PY * PZ;  // point pairs per thread
+    static_assert(PX == 2 || PX == 4, "a thread owns one or two x pairs of each row");
+    static_assert(LS == 1 || LS == 2 || LS == 4 || LS == 8, "lanes per patch");
+    constexpr int PPC = kDirectThreads / LS;  // patches per CTA
+    constexpr int HX = PX / 2;       // x pairs per row
+    constexpr int NP = HX * PY * PZ;  // point pairs per thread
     static_assert(EMU >= 0 && EMU <= NP, "EMU counts point pairs");
     static_assert(NP <= kDirectMaxPairs, "running totals do not fit");
     extern __shared__ __align__(128) unsigned char smem[];
@@ -107,7 +122,8 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
     const int split = p.split;
     const int rank = (int)(blockIdx.x % (unsigned)split);
     const long long ptile = blockIdx.x / (unsigned)split;
-    const long long patch = ptile * kDirectThreads + tid;
+    const int slice = tid % LS;  // this lane's share of each atom tile
+    const long long patch = ptile * PPC + tid / LS;
 
     // This CTA's slice of the atoms.
     const int a_begin = (int)((long long)p.n_atoms * rank / split);
@@ -115,17 +131,17 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
     const int n_local = a_end - a_begin;
     const int n_tiles = (n_local + kDirectTile - 1) / kDirectTile;
 
-    // This thread's patch: x quad qx, y block yb, z block zb (idle threads past
+    // This thread's patch: x group qx, y block yb, z block zb (idle threads past
     // the last patch compute a copy of it and store nothing).
     const long long pc = patch < p.npatch ? patch : p.npatch - 1;
     const int qx = (int)(pc % p.qx);
     const long long t = pc / p.qx;
     const int yb = (int)(t % p.yb);
     const int zb = (int)(t / p.yb);
-    const int i0 = 4 * qx, j0 = PY * yb, k0 = PZ * zb;
-    float x[4], y[PY], z[PZ];
+    const int i0 = PX * qx, j0 = PY * yb, k0 = PZ * zb;
+    float x[PX], y[PY], z[PZ];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) x[c] = fmaf((float)(i0 + c), p.h, p.ox);
+    for (int c = 0; c < PX; ++c) x[c] = fmaf((float)(i0 + c), p.h, p.ox);
 #pragma unroll
     for (int j = 0; j < PY; ++j) y[j] = fmaf((float)(j0 + j), p.h, p.oy);
 #pragma unroll
@@ -152,7 +168,7 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
         for (int s = 0; s < kDirectStages && s < n_tiles; ++s) issue(s, s);
     }
 
-    // Pair q = (k*PY + j)*2 + h is points (0,1) or (2,3) of row j, plane k.
+    // Pair q = (k*PY + j)*HX + h is points (0,1) or (2,3) of row j, plane k.
     // Each tile is summed in registers (part); the running totals stay in
     // shared memory (tot[q][tid]), which keeps registers for the pair loop.
     float2 *tot = reinterpret_cast<float2 *>(smem + kDirectRingBytes);
@@ -174,10 +190,11 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
         // 0,1 and 2,3; dy^2 + dz^2 duplicated per row), so only r^2, the
         // accumulate and the FMA-pipe rsqrt run as f32x2.
 #pragma unroll 2
-        for (int a = 0; a < n; ++a) {
-            const float4 at = tile[a];  // same address in every lane: broadcast
-            const float2 dx01 = make_float2(x[0] - at.x, x[1] - at.x);
-            const float2 dx23 = make_float2(x[2] - at.x, x[3] - at.x);
+        for (int a = slice; a < n; a += LS) {
+            const float4 at = tile[a];  // same address in the lanes of a slice: broadcast
+            float2 dxp[HX];
+#pragma unroll
+            for (int hh = 0; hh < HX; ++hh) dxp[hh] = make_float2(x[2 * hh] - at.x, x[2 * hh + 1] - at.x);
             const float2 q2 = make_float2(at.w, at.w);
             float dy2[PY];
 #pragma unroll
@@ -193,9 +210,9 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
                     const float d = fmaf(dz, dz, dy2[j]);
                     const float2 dyz2 = make_float2(d, d);
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int q = (k * PY + j) * 2 + hh;
-                        const float2 dx = hh == 0 ? dx01 : dx23;
+                    for (int hh = 0; hh < HX; ++hh) {
+                        const int q = (k * PY + j) * HX + hh;
+                        const float2 dx = dxp[hh];
                         const float2 r2 = __ffma2_rn(dx, dx, dyz2);
                         float2 rs;
                         if (q < EMU) {
@@ -217,55 +234,74 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
     float2 acc[NP];
 #pragma unroll
     for (int q = 0; q < NP; ++q) acc[q] = tot[q * kDirectThreads + tid];
+    if (LS > 1) {
+#pragma unroll
+        for (int q = 0; q < NP; ++q)
+#pragma unroll
+            for (int o = 1; o < LS; o <<= 1) {
+                acc[q].x += __shfl_xor_sync(0xffffffffu, acc[q].x, o);
+                acc[q].y += __shfl_xor_sync(0xffffffffu, acc[q].y, o);
+            }
+    }
     if (split == 1) {
-        if (patch < p.npatch) {
+        if (patch < p.npatch && slice == 0) {
 #pragma unroll
             for (int k = 0; k < PZ; ++k)
 #pragma unroll
                 for (int j = 0; j < PY; ++j) {
-                    const float2 a01 = acc[(k * PY + j) * 2], a23 = acc[(k * PY + j) * 2 + 1];
-                    store_quad<VEC>(p, i0, j0 + j, k0 + k, make_float4(a01.x, a01.y, a23.x, a23.y));
+                    const float2 a01 = acc[(k * PY + j) * HX];
+                    const float2 a23 = HX == 2 ? acc[(k * PY + j) * HX + HX - 1] : make_float2(0.f, 0.f);
+                    store_group<PX, VEC>(p, i0, j0 + j, k0 + k, make_float4(a01.x, a01.y, a23.x, a23.y));
                 }
         }
         return;
     }
 
-    // Cluster reduction: each thread's partial sums replace the running
-    // totals in this CTA's shared memory (same size: a float4 per patch row),
-    // then every element is summed over ranks 0..S-1, in rank order, by the
-    // CTA that owns it.
+    // Cluster reduction: each patch's partial sums replace the running
+    // totals in this CTA's shared memory (a float4 (PX = 4) or float2
+    // (PX = 2) per patch row, within the totals' space), then every element is
+    // summed over ranks 0..S-1, in rank order, by the CTA that owns it.
     constexpr int R = PY * PZ;
-    float4 *partial = reinterpret_cast<float4 *>(tot);  // [R][kDirectThreads]
+    using Group = typename std::conditional<PX == 4, float4, float2>::type;
+    Group *partial = reinterpret_cast<Group *>(tot);  // [R][PPC]
     __syncthreads();  // every thread has read its totals
+    if (slice == 0) {
 #pragma unroll
-    for (int k = 0; k < PZ; ++k)
+        for (int k = 0; k < PZ; ++k)
 #pragma unroll
-        for (int j = 0; j < PY; ++j) {
-            const float2 a01 = acc[(k * PY + j) * 2], a23 = acc[(k * PY + j) * 2 + 1];
-            partial[(k * PY + j) * kDirectThreads + tid] = make_float4(a01.x, a01.y, a23.x, a23.y);
-        }
+            for (int j = 0; j < PY; ++j) {
+                if constexpr (PX == 4) {
+                    const float2 a01 = acc[(k * PY + j) * 2], a23 = acc[(k * PY + j) * 2 + 1];
+                    partial[(k * PY + j) * PPC + tid / LS] = make_float4(a01.x, a01.y, a23.x, a23.y);
+                } else {
+                    partial[(k * PY + j) * PPC + tid / LS] = acc[k * PY + j];
+                }
+            }
+    }
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
-    const int n_elem = R * kDirectThreads;
+    const int n_elem = R * PPC;
     const int e_begin = n_elem * rank / split;
     const int e_end = n_elem * (rank + 1) / split;
     for (int e = e_begin + tid; e < e_end; e += kDirectThreads) {
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int r = 0; r < split; ++r) {
-            const float4 v = cluster.map_shared_rank(partial, r)[e];
+            const Group v = cluster.map_shared_rank(partial, r)[e];
             s.x += v.x;
             s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
+            if constexpr (PX == 4) {
+                s.z += v.z;
+                s.w += v.w;
+            }
         }
-        const int row = e / kDirectThreads;
-        const long long pe = ptile * kDirectThreads + (e % kDirectThreads);
+        const int row = e / PPC;
+        const long long pe = ptile * PPC + (e % PPC);
         if (pe < p.npatch) {
             const int eqx = (int)(pe % p.qx);
             const long long et = pe / p.qx;
             const int eyb = (int)(et % p.yb);
             const int ezb = (int)(et / p.yb);
-            store_quad<VEC>(p, 4 * eqx, PY * eyb + row % PY, PZ * ezb + row / PY, s);
+            store_group<PX, VEC>(p, PX * eqx, PY * eyb + row % PY, PZ * ezb + row / PY, s);
         }
     }
     cluster.sync();  // no CTA leaves while others still read its shared memory
@@ -278,21 +314,29 @@ namespace {
 
 using KernelFn = void (*)(DirectParams);
 
-// Patch shapes.  `rate` is the pair rate per SM clock each one reached on a
-// GB300 at full occupancy (best split on a 200^3 grid with 100k atoms, a
-// run of about 0.13 s); the planner uses it to rank the shapes.
+// Patch shapes (PX x points, PY rows, PZ planes; EMU point pairs with rsqrt
+// on the FMA pipe; LS lanes per patch).  `rate` is the pair rate per SM clock each one reached
+// on a GB300 at full occupancy (best split on a 200^3 grid with 100k atoms,
+// a run of about 0.13 s); the planner uses it to rank the shapes.  The
+// 2-point and shared-patch (LS > 1) shapes exist for grids with too few
+// 4-point patches to fill the GPU.
 struct Variant {
-    int py, pz, emu;
+    int px, py, pz, emu, ls;
     double rate;
     KernelFn vec, scalar;
 };
 
-#define CP_VARIANT(PY, PZ, EMU, RATE) \
-    {PY, PZ, EMU, RATE, direct_kernel<PY, PZ, EMU, true>, direct_kernel<PY, PZ, EMU, false>}
+#define CP_VARIANT(PX, PY, PZ, EMU, LS, RATE)                                                       \
+    {PX, PY, PZ, EMU, LS, RATE, direct_kernel<PX, PY, PZ, EMU, LS, true>,                           \
+     direct_kernel<PX, PY, PZ, EMU, LS, false>}
 const Variant kVariants[] = {
-    CP_VARIANT(4, 2, 0, 15.5), CP_VARIANT(2, 2, 0, 15.4), CP_VARIANT(4, 1, 0, 15.4), CP_VARIANT(2, 1, 0, 15.5),
-    CP_VARIANT(1, 1, 0, 15.3), CP_VARIANT(4, 2, 4, 17.8), CP_VARIANT(4, 2, 5, 17.9), CP_VARIANT(2, 2, 2, 19.3),
-    CP_VARIANT(4, 1, 2, 19.1), CP_VARIANT(2, 1, 1, 18.2),
+    CP_VARIANT(4, 4, 2, 0, 1, 15.46), CP_VARIANT(4, 2, 2, 0, 1, 15.44), CP_VARIANT(4, 4, 1, 0, 1, 15.36),
+    CP_VARIANT(4, 2, 1, 0, 1, 15.48), CP_VARIANT(4, 1, 1, 0, 1, 15.27), CP_VARIANT(4, 4, 2, 4, 1, 17.82),
+    CP_VARIANT(4, 4, 2, 5, 1, 17.87), CP_VARIANT(4, 2, 2, 2, 1, 19.23), CP_VARIANT(4, 4, 1, 2, 1, 19.07),
+    CP_VARIANT(4, 2, 1, 1, 1, 17.79), CP_VARIANT(2, 1, 1, 0, 1, 14.48), CP_VARIANT(2, 2, 1, 0, 1, 15.28),
+    CP_VARIANT(4, 1, 1, 0, 4, 15.29), CP_VARIANT(4, 1, 1, 0, 2, 15.33), CP_VARIANT(4, 2, 1, 1, 4, 18.00),
+    CP_VARIANT(4, 2, 1, 1, 2, 17.98), CP_VARIANT(4, 2, 1, 1, 8, 17.65), CP_VARIANT(4, 2, 2, 2, 4, 19.32),
+    CP_VARIANT(4, 4, 1, 2, 4, 19.30),
 };
 #undef CP_VARIANT
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
@@ -319,15 +363,16 @@ int resident_ctas(int v, int s, bool vec, const DeviceInfo &dev) {
     }
     if (s == 1) {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDirectThreads,
-                                                          direct_smem_bytes(kVariants[v].py, kVariants[v].pz)) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &per_sm, fn, kDirectThreads, direct_smem_bytes(kVariants[v].px, kVariants[v].py, kVariants[v].pz)) !=
+            cudaSuccess)
             return -1;
         slots = per_sm * dev.sm_count;
     } else {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(s * 64, 1, 1);
         cfg.blockDim = dim3(kDirectThreads, 1, 1);
-        cfg.dynamicSmemBytes = direct_smem_bytes(kVariants[v].py, kVariants[v].pz);
+        cfg.dynamicSmemBytes = direct_smem_bytes(kVariants[v].px, kVariants[v].py, kVariants[v].pz);
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
         attr.val.clusterDim.x = s;
@@ -354,6 +399,7 @@ int resident_ctas(int v, int s, bool vec, const DeviceInfo &dev) {
 struct Plan {
     int variant;
     int split;
+    bool vec;  // whole-group vector stores
     long long ptiles;
     int qx, yb;
     long long npatch;
@@ -364,20 +410,30 @@ struct Plan {
 // FMA latencies.
 double occupancy_factor(double warps) { return std::sqrt(std::min(1.0, warps / 24.0)); }
 
+// Whether variant v stores whole x groups as one vector: every row holds a
+// whole number of groups and V is aligned to a group (v_align: the largest
+// power of two, up to 16, dividing V's address).
+bool vector_stores(int v, const Grid &g, int v_align) {
+    const int px = kVariants[v].px;
+    return g.nx % px == 0 && v_align >= 4 * px;
+}
+
 // Picks the patch shape and cluster split with the smallest modelled time.
 // CTAs spread evenly over the SMs; the busiest SM runs ceil(CTAs / SMs) of
 // them, at most `resident` at a time, at the shape's measured pair rate
 // scaled by its occupancy; each split level adds a small reduction cost.
-int plan_direct(const Grid &g, int n_atoms, bool vec, const DeviceInfo &dev, Plan *out) {
+int plan_direct(const Grid &g, int n_atoms, int v_align, const DeviceInfo &dev, Plan *out) {
     double best = INFINITY;
     for (int v = 0; v < kNumVariants; ++v) {
-        const int py = kVariants[v].py, pz = kVariants[v].pz;
+        const int px = kVariants[v].px, py = kVariants[v].py, pz = kVariants[v].pz;
         if (pz > 1 && g.nz < pz) continue;
         if (py > 1 && g.ny < py) continue;
-        const long long qx = (g.nx + 3) / 4, yb = (g.ny + py - 1) / py, zb = (g.nz + pz - 1) / pz;
+        const bool vec = vector_stores(v, g, v_align);
+        const long long qx = (g.nx + px - 1) / px, yb = (g.ny + py - 1) / py, zb = (g.nz + pz - 1) / pz;
         const long long npatch = qx * yb * zb;
-        const long long ctas = (npatch + kDirectThreads - 1) / kDirectThreads;
-        const double pts = (double)kDirectThreads * 4 * py * pz;
+        const int ppc = kDirectThreads / kVariants[v].ls;  // patches per CTA
+        const long long ctas = (npatch + ppc - 1) / ppc;
+        const double pts = (double)ppc * px * py * pz;
         for (int s = 1; s <= kMaxSplit; ++s) {
             if (s == 5 || s == 7 || (s > 8 && s != 12 && s != 16)) continue;
             if (s > 1 && (long long)n_atoms < (long long)s * 64) break;
@@ -395,6 +451,7 @@ int plan_direct(const Grid &g, int n_atoms, bool vec, const DeviceInfo &dev, Pla
                 best = t;
                 out->variant = v;
                 out->split = s;
+                out->vec = vec;
                 out->ptiles = ctas;
                 out->qx = (int)qx;
                 out->yb = (int)yb;
@@ -412,22 +469,24 @@ int launch_direct(const float *atoms, int n_atoms, const Grid &g, float *V, cuda
     DeviceInfo dev;
     int rc = device_info(&dev);
     if (rc) return rc;
-    const bool vec = (g.nx % 4 == 0) && aligned(V, 16);
+    const int v_align = aligned(V, 16) ? 16 : aligned(V, 8) ? 8 : 4;
     Plan plan;
-    rc = plan_direct(g, n_atoms, vec, dev, &plan);
+    rc = plan_direct(g, n_atoms, v_align, dev, &plan);
     if (rc) return rc;
     if (force_variant >= 0 && force_variant < kNumVariants) {
         const int v = force_variant;
-        const int py = kVariants[v].py, pz = kVariants[v].pz;
+        const int px = kVariants[v].px, py = kVariants[v].py, pz = kVariants[v].pz;
         plan.variant = v;
-        plan.qx = (g.nx + 3) / 4;
+        plan.vec = vector_stores(v, g, v_align);
+        plan.qx = (g.nx + px - 1) / px;
         plan.yb = (g.ny + py - 1) / py;
         plan.npatch = (long long)plan.qx * plan.yb * ((g.nz + pz - 1) / pz);
-        plan.ptiles = (plan.npatch + kDirectThreads - 1) / kDirectThreads;
+        const int ppc = kDirectThreads / kVariants[v].ls;
+        plan.ptiles = (plan.npatch + ppc - 1) / ppc;
     }
     if (force_split >= 1 && force_split <= kMaxSplit) plan.split = force_split;
     if (plan.split > kPortableSplit) {  // sets the non-portable cluster attribute, checks support
-        const int slots = resident_ctas(plan.variant, plan.split, vec, dev);
+        const int slots = resident_ctas(plan.variant, plan.split, plan.vec, dev);
         if (slots < 0) return CP_ERR_CUDA;
         if (slots == 0) return CP_ERR_UNSUPPORTED;
     }
@@ -450,11 +509,12 @@ int launch_direct(const float *atoms, int n_atoms, const Grid &g, float *V, cuda
     p.status = device_status_ptr();
     if (!p.status) return CP_ERR_CUDA;
 
-    KernelFn fn = vec ? kVariants[plan.variant].vec : kVariants[plan.variant].scalar;
+    KernelFn fn = plan.vec ? kVariants[plan.variant].vec : kVariants[plan.variant].scalar;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(plan.ptiles * plan.split), 1, 1);
     cfg.blockDim = dim3(kDirectThreads, 1, 1);
-    cfg.dynamicSmemBytes = direct_smem_bytes(kVariants[plan.variant].py, kVariants[plan.variant].pz);
+    cfg.dynamicSmemBytes =
+        direct_smem_bytes(kVariants[plan.variant].px, kVariants[plan.variant].py, kVariants[plan.variant].pz);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -494,17 +554,16 @@ CP_API int cp_direct_plan(int n_atoms, int nx, int ny, int nz, int *variant, int
     rc = device_info(&dev);
     if (rc) return rc;
     Plan plan;
-    rc = plan_direct(g, n_atoms, nx % 4 == 0, dev, &plan);
+    rc = plan_direct(g, n_atoms, 16, dev, &plan);
     if (rc) return rc;
     *variant = plan.variant;
     *split = plan.split;
     return CP_OK;
 }
 
-// Same as cp_direct with the patch shape (index into the variant table:
-// 0 = 4x4x2, 1 = 4x2x2, 2 = 4x4x1, 3 = 4x2x1, 4 = 4x1x1 points) and the
-// cluster split forced (pass -1 / 0 to let the planner choose).  For tests
-// and tuning sweeps.
+// Same as cp_direct with the patch shape (index into the variant table
+// kVariants) and the cluster split forced (pass -1 / 0 to let the planner
+// choose).  For tests and tuning sweeps.
 CP_API int cp_direct_config(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
                             float *V, int variant, int split, void *stream) {
     Grid g;

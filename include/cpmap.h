@@ -101,11 +101,17 @@ CP_API int cp_direct(const float *atoms, int n_atoms, int nx, int ny, int nz, cp
 
 /* cp_direct with the per-thread point patch and the cluster split forced,
  * for tests and tuning sweeps.  variant: -1 = planner's choice, else a
- * patch of 4 x-points times PY rows times PZ planes, of whose 2*PY*PZ point
- * pairs the first EMU take their rsqrt on the FMA pipe instead of the SFU
- * ((PY, PZ, EMU)): 0 = (4,2,0), 1 = (2,2,0), 2 = (4,1,0), 3 = (2,1,0),
- * 4 = (1,1,0), 5 = (4,2,4), 6 = (4,2,5), 7 = (2,2,2), 8 = (4,1,2),
- * 9 = (2,1,1).  split: 0 = planner's choice, else 1..16 CTAs of a
+ * patch of PX x-points times PY rows times PZ planes, of whose (PX/2)*PY*PZ
+ * point pairs the first EMU take their rsqrt on the FMA pipe instead of the
+ * SFU, shared by LS neighbouring lanes that take every LS-th atom each
+ * ((PX, PY, PZ, EMU, LS)): 0 = (4,4,2,0,1), 1 = (4,2,2,0,1),
+ * 2 = (4,4,1,0,1), 3 = (4,2,1,0,1), 4 = (4,1,1,0,1), 5 = (4,4,2,4,1),
+ * 6 = (4,4,2,5,1), 7 = (4,2,2,2,1), 8 = (4,4,1,2,1), 9 = (4,2,1,1,1),
+ * 10 = (2,1,1,0,1), 11 = (2,2,1,0,1), 12 = (4,1,1,0,4), 13 = (4,1,1,0,2),
+ * 14 = (4,2,1,1,4), 15 = (4,2,1,1,2), 16 = (4,2,1,1,8), 17 = (4,2,2,2,4),
+ * 18 = (4,4,1,2,4) (the 2-point and shared-patch shapes
+ * serve grids too small for 4-point patches to fill the GPU).
+ * split: 0 = planner's choice, else 1..16 CTAs of a
  * cluster share one tile of points and take 1/split of the atoms each
  * (their partial sums meet in distributed shared memory; sizes above 8 use
  * non-portable clusters).  Results agree with cp_direct up to fp32

@@ -75,7 +75,7 @@ def test_direct_rejects_on_host(args, code):
 
 def test_direct_config_rejects_bad_variant():
     lib = cp.library()
-    assert lib.cp_direct_config(FAKE, 5, *GRID, FAKE, 10, 0, None) == -1
+    assert lib.cp_direct_config(FAKE, 5, *GRID, FAKE, len(cp.DIRECT_VARIANTS), 0, None) == -1
     assert lib.cp_direct_config(FAKE, 5, *GRID, FAKE, 0, 17, None) == -1
     assert lib.cp_direct_config(FAKE, 5, *GRID, FAKE, 0, -2, None) == -1
 

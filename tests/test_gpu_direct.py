@@ -70,6 +70,25 @@ def test_direct_unaligned_output_and_odd_nx():
     assert_within_bound(out.cpu().numpy(), ref, bound)
 
 
+@pytest.mark.parametrize("variant", sorted(cp.DIRECT_VARIANTS))
+@pytest.mark.parametrize("shape,offset", [((13, 7, 5), 1), ((18, 5, 4), 2)])
+def test_direct_every_variant_store_paths(variant, shape, offset):
+    """Odd nx into a 4-byte aligned output (scalar stores for every shape), and
+    nx = 18 into an 8-byte aligned output (float2 stores for the 2-point shapes,
+    scalar ones for the 4-point shapes), without and with a 16-CTA split; the
+    floats around the output stay untouched."""
+    n = shape[0] * shape[1] * shape[2]
+    w = workloads.random_case(400 + variant, 700, shape, h=0.5, margin=1.0)
+    ref, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+    for split in (1, 16):
+        buf = torch.full((n + offset + 1,), float("nan"), device="cuda")
+        out = buf[offset:offset + n]
+        cp.direct(to_dev(w.atoms), w.shape, w.origin, w.h, out=out, variant=variant, split=split)
+        torch.cuda.synchronize()
+        assert torch.isnan(buf[:offset]).all().item() and torch.isnan(buf[-1]).item()
+        assert_within_bound(out.cpu().numpy(), ref, bound, f"variant {variant} split {split}")
+
+
 def test_direct_overwrites_output():
     w = workloads.random_case(8, 300, (16, 8, 4), margin=1.0)
     out = torch.full((4, 8, 16), 1e30, device="cuda")
