@@ -27,7 +27,9 @@
 //   * accuracy: each tile's contribution is summed in separate registers and
 //     then added to a running total kept in shared memory, so the fp32
 //     rounding error grows like (tile + n_atoms / tile) instead of n_atoms;
-//   * small grids: when there are too few point patches to fill the GPU, S
+//   * small grids: when there are too few point patches to fill the GPU,
+//     LS = 2, 4 or 8 neighbouring lanes share a patch and take every LS-th
+//     atom of each tile (a fixed xor-shuffle tree adds their sums), and S
 //     CTAs of a thread-block cluster share one tile of points and take 1/S
 //     of the atoms each; their partial sums meet in distributed shared
 //     memory and are added in rank order (deterministic, no atomics, no
