@@ -16,8 +16,8 @@
 //     stores 32 consecutive float4s (float2s) of a row (section 18.4 and the article's
 //     coarsen-plus-coalesce kernel, section 三);
 //   * atom tiles: instead of 4K-atom chunks in constant memory re-launched
-//     per chunk (section 18.2), one launch streams 256-atom tiles from global
-//     memory into a 3-stage shared-memory ring with 1-D TMA bulk copies; all
+//     per chunk (section 18.2), one launch streams 512-atom tiles from global
+//     memory into a 2-stage shared-memory ring with 1-D TMA bulk copies; all
 //     threads read the same atom (a shared-memory broadcast);
 //   * f32x2: a thread's x points are register pairs, so r^2, the
 //     accumulate and the FMA-pipe rsqrt are paired Blackwell instructions;
@@ -50,8 +50,8 @@ namespace cg = cooperative_groups;
 namespace cpmap {
 
 constexpr int kDirectThreads = 128;
-constexpr int kDirectTile = 256;  // atoms per shared-memory stage (4 KiB as loaded)
-constexpr int kDirectStages = 3;
+constexpr int kDirectTile = 512;  // atoms per shared-memory stage (8 KiB as loaded)
+constexpr int kDirectStages = 2;
 // dynamic shared memory: the TMA ring of atoms, then every thread's running
 // totals (up to 16 point pairs of 8 bytes)
 constexpr int kDirectRingBytes = kDirectStages * kDirectTile * 16;
@@ -333,12 +333,12 @@ struct Variant {
      direct_kernel<PX, PY, PZ, EMU, LS, false>}
 const Variant kVariants[] = {
     CP_VARIANT(4, 4, 2, 0, 1, 15.46), CP_VARIANT(4, 2, 2, 0, 1, 15.44), CP_VARIANT(4, 4, 1, 0, 1, 15.36),
-    CP_VARIANT(4, 2, 1, 0, 1, 15.48), CP_VARIANT(4, 1, 1, 0, 1, 15.27), CP_VARIANT(4, 4, 2, 4, 1, 17.82),
-    CP_VARIANT(4, 4, 2, 5, 1, 17.87), CP_VARIANT(4, 2, 2, 2, 1, 19.23), CP_VARIANT(4, 4, 1, 2, 1, 19.07),
-    CP_VARIANT(4, 2, 1, 1, 1, 17.79), CP_VARIANT(2, 1, 1, 0, 1, 14.48), CP_VARIANT(2, 2, 1, 0, 1, 15.28),
-    CP_VARIANT(4, 1, 1, 0, 4, 15.29), CP_VARIANT(4, 1, 1, 0, 2, 15.33), CP_VARIANT(4, 2, 1, 1, 4, 18.00),
-    CP_VARIANT(4, 2, 1, 1, 2, 17.98), CP_VARIANT(4, 2, 1, 1, 8, 17.65), CP_VARIANT(4, 2, 2, 2, 4, 19.32),
-    CP_VARIANT(4, 4, 1, 2, 4, 19.30),
+    CP_VARIANT(4, 2, 1, 0, 1, 15.48), CP_VARIANT(4, 1, 1, 0, 1, 15.31), CP_VARIANT(4, 4, 2, 4, 1, 17.82),
+    CP_VARIANT(4, 4, 2, 5, 1, 17.87), CP_VARIANT(4, 2, 2, 2, 1, 19.21), CP_VARIANT(4, 4, 1, 2, 1, 18.93),
+    CP_VARIANT(4, 2, 1, 1, 1, 17.87), CP_VARIANT(2, 1, 1, 0, 1, 14.48), CP_VARIANT(2, 2, 1, 0, 1, 15.28),
+    CP_VARIANT(4, 1, 1, 0, 4, 15.35), CP_VARIANT(4, 1, 1, 0, 2, 15.33), CP_VARIANT(4, 2, 1, 1, 4, 17.97),
+    CP_VARIANT(4, 2, 1, 1, 2, 17.98), CP_VARIANT(4, 2, 1, 1, 8, 17.82), CP_VARIANT(4, 2, 2, 2, 4, 19.50),
+    CP_VARIANT(4, 4, 1, 2, 4, 19.59),
 };
 #undef CP_VARIANT
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
