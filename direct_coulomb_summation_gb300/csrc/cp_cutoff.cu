@@ -17,7 +17,7 @@
 // per 8x8x8-point brick, a producer warp and four consumer warps.
 //   * The producer walks the brick's neighbourhood offset list (one x-run of
 //     bins per (dy, dz), passed as a kernel parameter) and packs the atoms
-//     into a ring of 128-atom shared-memory stages with 1-D TMA bulk copies:
+//     into a ring of 8 shared-memory stages of 192 atoms with 1-D TMA bulk copies:
 //     with capacity 0 each run is one contiguous range of the bin-sorted
 //     array; with capacity 8 or 16 it is the run's fixed-capacity slots
 //     (trimmed to its occupied bins), then the overflow of every bin holding
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(256) bin_sort_pack_lane_kernel(const __grid_co
 
 constexpr int kBrickConsumerWarps = 4;
 constexpr int kBrickThreads = 32 * (kBrickConsumerWarps + 1);  // + 1 producer warp
-constexpr int kBrickStages = 12;
+constexpr int kBrickStages = 8;
 
 struct BrickParams {
     int nx, ny, nz;
@@ -349,7 +349,7 @@ __device__ __forceinline__ int brick_home_dev(int brick, int m, double h, double
 // Atoms per shared-memory stage.  The producer packs as many bin runs (or
 // pieces of runs) into a stage as fit, so a stage usually holds several
 // runs; every consumer warp tests the whole stage against its own sub-box.
-constexpr int kStageAtoms = 128;
+constexpr int kStageAtoms = 192;
 
 template <int K, bool VEC, bool COUNT>
 __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __grid_constant__ BrickParams p) {
