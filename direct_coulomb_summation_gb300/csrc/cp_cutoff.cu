@@ -877,13 +877,13 @@ constexpr size_t kStaticWorkspaceBytes = size_t(16) << 20;  // 16 MiB per device
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
 std::mutex g_static_ws_mutex;
-void *g_static_ws_ptr[64];
+void *g_static_ws_ptr[kMaxDevices];
 
 // Device address of g_static_workspace on the current device, looked up
 // once per device (the first call on each device does it).
 void *static_workspace_ptr() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_static_ws_mutex);
     if (!g_static_ws_ptr[dev]) {
         void *p = nullptr;

@@ -348,7 +348,7 @@ constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 // sizes above 8 it also sets the non-portable cluster attribute of that
 // exact kernel, which the launch needs.
 std::mutex g_plan_mutex;
-int g_slots[64][kNumVariants][2][kMaxSplit + 1];  // [device][variant][vector stores][split]
+int g_slots[kMaxDevices][kNumVariants][2][kMaxSplit + 1];  // [device][variant][vector stores][split]
 
 int resident_ctas(int v, int s, bool vec, const DeviceInfo &dev) {
     std::lock_guard<std::mutex> lock(g_plan_mutex);

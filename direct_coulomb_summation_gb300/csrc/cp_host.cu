@@ -207,7 +207,6 @@ int make_layout(int n_atoms, const BinGeom &bg, int capacity, cp_cutoff_layout *
 
 namespace {
 std::mutex g_dev_mutex;
-constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ok[kMaxDevices];
 unsigned int *g_status_ptr[kMaxDevices];

@@ -61,6 +61,10 @@ int make_layout(int n_atoms, const BinGeom &bg, int capacity, cp_cutoff_layout *
 int sort_atoms_into_cells(const float4 *atoms, int n_atoms, const BinGeom &bg, const cp_cutoff_layout &L,
                           void *workspace, cudaStream_t stream);
 
+// Devices the library keeps per-device state for (ordinals 0 .. kMaxDevices-1;
+// calls on a device past that return CP_ERR_CUDA).
+constexpr int kMaxDevices = 64;
+
 struct DeviceInfo {
     int device;
     int sm_count;
