@@ -506,9 +506,9 @@ def run_ours(args):
     peak_direct = per_sm_direct * sm_clk
     achieved_direct = direct_rate
     # the same pair with its rsqrt split between the SFU and the FMA pipe
-    # (estimate + two Newton steps: 7 FP32 ops): best split f solves
-    # (1 - f)/R_sfu = (3 + 7f)/R_fp32
-    f_split = (r_ffma - 3.0 * r_mufu) / (r_ffma + 7.0 * r_mufu)
+    # (estimate + two Newton steps: 6 FP32 ops): best split f solves
+    # (1 - f)/R_sfu = (3 + 6f)/R_fp32
+    f_split = (r_ffma - 3.0 * r_mufu) / (r_ffma + 6.0 * r_mufu)
     per_sm_split = r_mufu / (1.0 - f_split)
     # cutoff: a useful pair needs 1 SFU rsqrt and about 11 FP32 ops (dx, dy,
     # dz, three for r^2, compare, two for g, subtract, accumulate):
@@ -589,9 +589,9 @@ def run_ours(args):
             "traffic": traffic,
             "peak_basis": f"{n_sm} SMs x {per_sm_split:.1f} pairs/clk/SM x {f_mhz:.0f} MHz ({clock_basis}): "
                           f"the pair (1 rsqrt, 3 FP32 ops) with its rsqrt shared between the SFU ({r_mufu:.2f}/clk/SM "
-                          f"measured) and the FMA pipe (magic-constant estimate + two Newton steps, 7 FP32 ops; "
+                          f"measured) and the FMA pipe (magic-constant estimate + two Newton steps, 6 FP32 ops; "
                           f"FFMA {r_ffma:.1f} lanes/clk/SM measured) at the best share {f_split:.2f}, "
-                          f"(1 - f)/R_sfu = (3 + 7f)/R_fp32",
+                          f"(1 - f)/R_sfu = (3 + 6f)/R_fp32",
             "peak_sfu_only": peak_direct,
             "frac_sfu_only": achieved_direct / peak_direct,
             "sfu_only_basis": f"{n_sm} SMs x {per_sm_direct:.2f} pairs/clk/SM = min(SFU rsqrt {r_mufu:.2f}, "

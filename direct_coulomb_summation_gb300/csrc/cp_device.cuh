@@ -35,21 +35,29 @@ __device__ __forceinline__ float sfu_rsqrt(float x) {
 }
 
 // Two reciprocal square roots on the FMA pipe instead of the SFU, for
-// positive normal inputs: the initial estimate of the "fast inverse square
-// root" (integer 0x5f3759df - bits/2; C. Lomont, "Fast Inverse Square Root",
-// 2003) refined by two Newton steps y <- y * (3/2 - (x/2) y^2), done on
-// f32x2 pairs.  After the first step the relative error is below 1.8e-3,
-// after the second below 5e-6 (the Newton error roughly squares, times
-// 3/2, plus fp32 rounding).
-__device__ __forceinline__ float2 fma_rsqrt2(float2 x) {
-    float2 y = make_float2(__int_as_float(0x5f3759df - (__float_as_int(x.x) >> 1)),
-                           __int_as_float(0x5f3759df - (__float_as_int(x.y) >> 1)));
-    const float2 nhx = __fmul2_rn(x, make_float2(-0.5f, -0.5f));
-    const float2 c15 = make_float2(1.5f, 1.5f);
-    y = __fmul2_rn(y, __ffma2_rn(nhx, __fmul2_rn(y, y), c15));
-    y = __fmul2_rn(y, __ffma2_rn(nhx, __fmul2_rn(y, y), c15));
-    return y;
+// positive normal inputs, returned divided by sqrt(2): v = rsqrt(x)/sqrt(2).
+// The initial estimate is that of the "fast inverse square root" (integer
+// 0x5f3759df - bits/2; C. Lomont, "Fast Inverse Square Root", 2003) with
+// 2^22 taken off the constant, which halves it in the log domain, i.e.
+// divides it by about sqrt(2).  Newton's step y <- y (3/2 - (x/2) y^2) for
+// y = sqrt(2) v reads v <- v (3/2 - x v^2): it needs x itself rather than
+// x/2, and written as v <- v (x v^2 - 3/2) it needs no negated operand
+// either (the sign of v flips at each step, and two steps restore it).  So
+// two steps cost 6 f32x2 operations instead of 7.  Relative error after the
+// second step below 5e-6 (the Newton error roughly squares, times 3/2, plus
+// fp32 rounding; 4.75e-6 over every fp32 in [1, 4), and the error repeats
+// every factor of 4).  The caller multiplies by sqrt(2) once per sum.
+__device__ __forceinline__ float2 fma_rsqrt2_scaled(float2 x) {
+    float2 v = make_float2(__int_as_float(0x5ef759df - (__float_as_int(x.x) >> 1)),
+                           __int_as_float(0x5ef759df - (__float_as_int(x.y) >> 1)));
+    const float2 m15 = make_float2(-1.5f, -1.5f);
+    v = __fmul2_rn(v, __ffma2_rn(x, __fmul2_rn(v, v), m15));
+    v = __fmul2_rn(v, __ffma2_rn(x, __fmul2_rn(v, v), m15));
+    return v;
 }
+
+// sqrt(2) rounded to fp32: undoes the scaling of fma_rsqrt2_scaled.
+constexpr float kSqrt2 = 1.41421356f;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

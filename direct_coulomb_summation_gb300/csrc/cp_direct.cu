@@ -22,7 +22,7 @@
 //   * f32x2: a thread's x points are register pairs, so r^2, the
 //     accumulate and the FMA-pipe rsqrt are paired Blackwell instructions;
 //   * rsqrt on two pipes: a compile-time share of each thread's point pairs
-//     takes its rsqrt on the FMA pipe (fma_rsqrt2) and the rest on the SFU,
+//     takes its rsqrt on the FMA pipe (fma_rsqrt2_scaled) and the rest on the SFU,
 //     so that neither unit alone limits the pair rate;
 //   * accuracy: each tile's contribution is summed in separate registers and
 //     then added to a running total kept in shared memory, so the fp32
@@ -103,7 +103,7 @@ __device__ __forceinline__ void store_group(const DirectParams &p, int i0, int y
 
 // A patch is PX x points (PX/2 f32x2 pairs) x PY rows x PZ planes, i.e.
 // (PX/2)*PY*PZ point pairs.  The first EMU pairs take their rsqrt on the FMA
-// pipe (fma_rsqrt2), the others on the SFU, so that both units share the work.
+// pipe (fma_rsqrt2_scaled), the others on the SFU, so that both units share the work.
 // LS neighbouring lanes share a patch, each taking every LS-th atom of a tile
 // (more warps for grids with few patches); their sums meet by a fixed
 // xor-shuffle tree, so every lane of the group holds the same total.
@@ -198,18 +198,22 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
 #pragma unroll
             for (int hh = 0; hh < HX; ++hh) dxp[hh] = make_float2(x[2 * hh] - at.x, x[2 * hh + 1] - at.x);
             const float2 q2 = make_float2(at.w, at.w);
-            float dy2[PY];
+            // dy^2 + dz^2 per row: the square of the shorter axis is taken
+            // once and the other axis fused into it (PY + PZ*PY operations
+            // when PZ >= PY, PZ + PY*PZ otherwise)
+            float dy[PY], dy2[PY];
 #pragma unroll
             for (int j = 0; j < PY; ++j) {
-                const float dy = y[j] - at.y;
-                dy2[j] = dy * dy;
+                dy[j] = y[j] - at.y;
+                dy2[j] = dy[j] * dy[j];
             }
 #pragma unroll
             for (int k = 0; k < PZ; ++k) {
                 const float dz = z[k] - at.z;
+                const float dz2 = dz * dz;
 #pragma unroll
                 for (int j = 0; j < PY; ++j) {
-                    const float d = fmaf(dz, dz, dy2[j]);
+                    const float d = PZ < PY ? fmaf(dy[j], dy[j], dz2) : fmaf(dz, dz, dy2[j]);
                     const float2 dyz2 = make_float2(d, d);
 #pragma unroll
                     for (int hh = 0; hh < HX; ++hh) {
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
                         const float2 r2 = __ffma2_rn(dx, dx, dyz2);
                         float2 rs;
                         if (q < EMU) {
-                            rs = fma_rsqrt2(r2);
+                            rs = fma_rsqrt2_scaled(r2);  // rsqrt / sqrt(2): scaled back per tile
                         } else {
                             rs = make_float2(sfu_rsqrt(r2.x), sfu_rsqrt(r2.y));
                         }
@@ -228,7 +232,10 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
             }
         }
 #pragma unroll
-        for (int q = 0; q < NP; ++q) tot[q * kDirectThreads + tid] = __fadd2_rn(tot[q * kDirectThreads + tid], part[q]);
+        for (int q = 0; q < NP; ++q) {
+            const float2 pq = q < EMU ? __fmul2_rn(part[q], make_float2(kSqrt2, kSqrt2)) : part[q];
+            tot[q * kDirectThreads + tid] = __fadd2_rn(tot[q * kDirectThreads + tid], pq);
+        }
         __syncthreads();  // every thread is done with this stage
         if (tid == 0 && it + kDirectStages < n_tiles) issue(it + kDirectStages, stage);
     }
@@ -332,13 +339,13 @@ struct Variant {
     {PX, PY, PZ, EMU, LS, RATE, direct_kernel<PX, PY, PZ, EMU, LS, true>,                           \
      direct_kernel<PX, PY, PZ, EMU, LS, false>}
 const Variant kVariants[] = {
-    CP_VARIANT(4, 4, 2, 0, 1, 15.46), CP_VARIANT(4, 2, 2, 0, 1, 15.44), CP_VARIANT(4, 4, 1, 0, 1, 15.36),
-    CP_VARIANT(4, 2, 1, 0, 1, 15.48), CP_VARIANT(4, 1, 1, 0, 1, 15.31), CP_VARIANT(4, 4, 2, 4, 1, 17.82),
-    CP_VARIANT(4, 4, 2, 5, 1, 17.87), CP_VARIANT(4, 2, 2, 2, 1, 19.21), CP_VARIANT(4, 4, 1, 2, 1, 18.93),
-    CP_VARIANT(4, 2, 1, 1, 1, 17.87), CP_VARIANT(2, 1, 1, 0, 1, 14.48), CP_VARIANT(2, 2, 1, 0, 1, 15.28),
-    CP_VARIANT(4, 1, 1, 0, 4, 15.35), CP_VARIANT(4, 1, 1, 0, 2, 15.33), CP_VARIANT(4, 2, 1, 1, 4, 17.97),
-    CP_VARIANT(4, 2, 1, 1, 2, 17.98), CP_VARIANT(4, 2, 1, 1, 8, 17.82), CP_VARIANT(4, 2, 2, 2, 4, 19.50),
-    CP_VARIANT(4, 4, 1, 2, 4, 19.59),
+    CP_VARIANT(4, 4, 2, 0, 1, 15.48), CP_VARIANT(4, 2, 2, 0, 1, 15.47), CP_VARIANT(4, 4, 1, 0, 1, 15.41),
+    CP_VARIANT(4, 2, 1, 0, 1, 15.58), CP_VARIANT(4, 1, 1, 0, 1, 15.31), CP_VARIANT(4, 4, 2, 4, 1, 18.96),
+    CP_VARIANT(4, 4, 2, 5, 1, 19.40), CP_VARIANT(4, 2, 2, 2, 1, 19.28), CP_VARIANT(4, 4, 1, 2, 1, 19.39),
+    CP_VARIANT(4, 2, 1, 1, 1, 18.81), CP_VARIANT(2, 1, 1, 0, 1, 14.57), CP_VARIANT(2, 2, 1, 0, 1, 15.32),
+    CP_VARIANT(4, 1, 1, 0, 4, 15.35), CP_VARIANT(4, 1, 1, 0, 2, 15.36), CP_VARIANT(4, 2, 1, 1, 4, 18.87),
+    CP_VARIANT(4, 2, 1, 1, 2, 18.94), CP_VARIANT(4, 2, 1, 1, 8, 18.73), CP_VARIANT(4, 2, 2, 2, 4, 19.69),
+    CP_VARIANT(4, 4, 1, 2, 4, 19.89),
 };
 #undef CP_VARIANT
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);

@@ -81,7 +81,7 @@ __global__ void eval_rsqrt_kernel(const float *x, float *y, int n) {
     if (KIND == 0)
         r = make_float2(sfu_rsqrt(v.x), sfu_rsqrt(v.y));
     else
-        r = fma_rsqrt2(v);
+        r = __fmul2_rn(fma_rsqrt2_scaled(v), make_float2(kSqrt2, kSqrt2));
     y[i] = r.x;
     if (i + 1 < n) y[i + 1] = r.y;
 }

@@ -445,8 +445,8 @@ CP_API int cp_version(void);
 /* Evaluates n reciprocal square roots of the DEVICE array x into the DEVICE
  * array y with one of the kernels' two routes: kind 0 = the SFU
  * (rsqrt.approx.ftz.f32), kind 1 = the FMA-pipe route (magic-constant
- * estimate and two Newton steps, relative error below 5e-6 for positive
- * normal x).  For tests of those error bounds.  Returns CP_OK,
+ * estimate and two Newton steps on rsqrt(x)/sqrt(2), then times fp32
+ * sqrt(2); relative error below 5e-6 for positive normal x).  For tests of those error bounds.  Returns CP_OK,
  * CP_ERR_INVALID_ARGUMENT or CP_ERR_CUDA.                                    */
 CP_API int cp_eval_rsqrt(int kind, const float *x, float *y, int n, void *stream);
 
