@@ -139,3 +139,30 @@ def test_maximum_grid():
     assert cp.device_status() == 0
     del V, flat
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 37, 1), (2, 1, 9), (3, 3, 3), (1000, 1, 1), (1, 1, 300),
+                                   (5, 1, 64)])
+def test_degenerate_grids(shape):
+    """Grids one or two points wide along some axes: the planner's choice, the
+    shared-patch and 2-point shapes with and without a cluster split (rows and
+    planes past the grid are computed and not stored), and the cutoff map, each
+    against the oracle at every point."""
+    w = workloads.random_case(90 + sum(shape), 500, shape, h=0.5, origin=(-1.0, 2.0, 0.5), margin=3.0)
+    a = to_dev(w.atoms)
+    ref, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+    V = cp.direct(a, w.shape, w.origin, w.h)
+    torch.cuda.synchronize()
+    assert_within_bound(V.cpu().numpy(), ref, bound, f"{shape} planner")
+    for v in (10, 12, 16, 17, 18):
+        for split in (1, 5):
+            V = cp.direct(a, w.shape, w.origin, w.h, variant=v, split=split)
+            torch.cuda.synchronize()
+            assert_within_bound(V.cpu().numpy(), ref, bound, f"{shape} variant {v} split {split}")
+    c, b = 2.5, 1.0
+    refc, boundc = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, c)
+    for K in (0, 16):
+        Vc = cp.cutoff(a, w.shape, w.origin, w.h, c, b, capacity=K)
+        torch.cuda.synchronize()
+        assert_within_bound(Vc.cpu().numpy(), refc, boundc, f"{shape} cutoff K={K}")
+    assert cp.device_status() == 0
