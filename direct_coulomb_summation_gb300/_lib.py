@@ -78,6 +78,7 @@ SIGNATURES = {
     "cp_direct": (_I, [_P, _I, *_GRID, _P, _P]),
     "cp_direct_config": (_I, [_P, _I, *_GRID, _P, _I, _I, _P]),
     "cp_direct_plan": (_I, [_I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "cp_grid_points_exact": (_I, [_I, _I, _I, cp_vec3, _F]),
     "cp_cutoff_layout_of": (_I, [_I, *_GRID, _F, _F, _I, ctypes.POINTER(cp_cutoff_layout)]),
     "cp_cutoff_workspace_bytes": (_SZ, [_I, *_GRID, _F, _F, _I]),
     "cp_cutoff": (_I, [_P, _I, *_GRID, _F, _F, _I, _P, _SZ, _P, _P]),

@@ -351,7 +351,11 @@ __device__ __forceinline__ int brick_home_dev(int brick, int m, double h, double
 // runs; every consumer warp tests the whole stage against its own sub-box.
 constexpr int kStageAtoms = 192;
 
-template <int K, bool VEC, bool COUNT>
+// REL: the grid points are not all exact in fp32, so the lists hold
+// origin - atom and differences are formed relative to the grid origin;
+// otherwise the lists hold the atoms and differences are point - atom, which
+// then rounds only once.
+template <int K, bool VEC, bool COUNT, bool REL>
 __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __grid_constant__ BrickParams p) {
     __shared__ __align__(128) float4 ring[kBrickStages][kStageAtoms];
     // each consumer warp's list of the stage's atoms that can reach its
@@ -500,11 +504,17 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
     const int yy = (warp & 1) * 4 + ((lane >> 1) & 3);
     const int zz = (warp >> 1) * 4 + (lane >> 3);
     const int i0 = kBrick * bx + xq, j = kBrick * by + yy, k = kBrick * bz + zz;
+    // REL: the lane's grid indices, and a difference to a listed atom is
+    // formed as index * h + (origin - atom) with one rounding (the list
+    // holds origin - atom), so its error follows the atom's offset from the
+    // grid origin, not the grid's distance from the coordinate origin.
+    // Otherwise the points' coordinates, exact in fp32, and point - atom.
     float x[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) x[c] = fmaf((float)(i0 + c), p.h, p.ox);
-    const float y = fmaf((float)j, p.h, p.oy);
-    const float z = fmaf((float)k, p.h, p.oz);
+    for (int c = 0; c < 4; ++c) x[c] = REL ? (float)(i0 + c) : fmaf((float)(i0 + c), p.h, p.ox);
+    const float y = REL ? (float)j : fmaf((float)j, p.h, p.oy);
+    const float z = REL ? (float)k : fmaf((float)k, p.h, p.oz);
+    auto diff = [&](float u, float a) { return REL ? fmaf(u, p.h, a) : u - a; };
     const float2 NG0 = make_float2(-p.gc0, -p.gc0), NG1 = make_float2(-p.gc1, -p.gc1);
     const float2 NG2 = make_float2(-p.gc2, -p.gc2);
     // this warp's sub-box: all 8 x, 4 y rows, 4 z planes
@@ -535,7 +545,8 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
             const float ez = fmaxf(fmaxf(loz - a.z, a.z - hiz), 0.0f);
             const bool near = fmaf(ez, ez, fmaf(ey, ey, ex * ex)) < p.cull2;
             const unsigned m = __ballot_sync(0xffffffffu, near);
-            if (near && CP_IN(cnt + __popc(m & below), kStageAtoms, p.status)) list[cnt + __popc(m & below)] = a;
+            if (near && CP_IN(cnt + __popc(m & below), kStageAtoms, p.status))
+                list[cnt + __popc(m & below)] = REL ? make_float4(p.ox - a.x, p.oy - a.y, p.oz - a.z, a.w) : a;
             cnt += __popc(m);
         }
         __syncwarp();
@@ -548,11 +559,11 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
             const float4 a = list[t];  // broadcast
             // differences as scalars (dy^2 + dz^2 is the same for the
             // lane's 4 points), written into the f32x2 operand pairs
-            const float dy = y - a.y, dz = z - a.z;
+            const float dy = diff(y, a.y), dz = diff(z, a.z);
             const float d = fmaf(dy, dy, dz * dz);
             const float2 dyz2 = make_float2(d, d);
-            const float2 dx01 = make_float2(x[0] - a.x, x[1] - a.x);
-            const float2 dx23 = make_float2(x[2] - a.x, x[3] - a.x);
+            const float2 dx01 = make_float2(diff(x[0], a.x), diff(x[1], a.x));
+            const float2 dx23 = make_float2(diff(x[2], a.x), diff(x[3], a.x));
             const float2 r01 = __ffma2_rn(dx01, dx01, dyz2);
             const float2 r23 = __ffma2_rn(dx23, dx23, dyz2);
             // e = rsqrt(r^2) - g(r^2), with -g by Horner on the negated coefficients
@@ -736,12 +747,20 @@ int launch_bricks_k(const Prepared &P, const OffsetList &L, float *V, cudaStream
     const long long nbricks = (long long)p.nbr[0] * p.nbr[1] * p.nbr[2];
     if (nbricks > 0x7fffffffll) return CP_ERR_TOO_LARGE;
     const bool vec = V && (g.nx % 4 == 0) && aligned(V, 16);
-    if (counts)
-        cutoff_brick_kernel<K, false, true><<<(unsigned)nbricks, kBrickThreads, 0, stream>>>(p);
+    const bool rel = !grid_points_exact(g);
+    const unsigned nb = (unsigned)nbricks;
+    if (counts && rel)
+        cutoff_brick_kernel<K, false, true, true><<<nb, kBrickThreads, 0, stream>>>(p);
+    else if (counts)
+        cutoff_brick_kernel<K, false, true, false><<<nb, kBrickThreads, 0, stream>>>(p);
+    else if (vec && rel)
+        cutoff_brick_kernel<K, true, false, true><<<nb, kBrickThreads, 0, stream>>>(p);
     else if (vec)
-        cutoff_brick_kernel<K, true, false><<<(unsigned)nbricks, kBrickThreads, 0, stream>>>(p);
+        cutoff_brick_kernel<K, true, false, false><<<nb, kBrickThreads, 0, stream>>>(p);
+    else if (rel)
+        cutoff_brick_kernel<K, false, false, true><<<nb, kBrickThreads, 0, stream>>>(p);
     else
-        cutoff_brick_kernel<K, false, false><<<(unsigned)nbricks, kBrickThreads, 0, stream>>>(p);
+        cutoff_brick_kernel<K, false, false, false><<<nb, kBrickThreads, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
     note_launches(1);
     return CP_OK;

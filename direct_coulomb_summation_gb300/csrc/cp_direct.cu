@@ -107,7 +107,10 @@ __device__ __forceinline__ void store_group(const DirectParams &p, int i0, int y
 // LS neighbouring lanes share a patch, each taking every LS-th atom of a tile
 // (more warps for grids with few patches); their sums meet by a fixed
 // xor-shuffle tree, so every lane of the group holds the same total.
-template <int PX, int PY, int PZ, int EMU, int LS, bool VEC>
+// REL: the grid points are not all exact in fp32, so differences are formed
+// relative to the grid origin (see below); otherwise point - atom, which
+// then rounds only once.
+template <int PX, int PY, int PZ, int EMU, int LS, bool VEC, bool REL>
 __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_constant__ DirectParams p) {
     static_assert(PX == 2 || PX == 4, "a thread owns one or two x pairs of each row");
     static_assert(LS == 1 || LS == 2 || LS == 4 || LS == 8, "lanes per patch");
@@ -141,13 +144,21 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
     const int yb = (int)(t % p.yb);
     const int zb = (int)(t / p.yb);
     const int i0 = PX * qx, j0 = PY * yb, k0 = PZ * zb;
+    // REL: the points' grid indices, and a difference to an atom is formed
+    // as index * h + (origin - atom) with one rounding (the fused multiply-add
+    // keeps index * h exact), so its error follows the atom's offset from the
+    // grid origin, not the grid's distance from the coordinate origin.
+    // Otherwise the points' coordinates, exact in fp32, and point - atom.
     float x[PX], y[PY], z[PZ];
 #pragma unroll
-    for (int c = 0; c < PX; ++c) x[c] = fmaf((float)(i0 + c), p.h, p.ox);
+    for (int c = 0; c < PX; ++c) x[c] = REL ? (float)(i0 + c) : fmaf((float)(i0 + c), p.h, p.ox);
 #pragma unroll
-    for (int j = 0; j < PY; ++j) y[j] = fmaf((float)(j0 + j), p.h, p.oy);
+    for (int j = 0; j < PY; ++j) y[j] = REL ? (float)(j0 + j) : fmaf((float)(j0 + j), p.h, p.oy);
 #pragma unroll
-    for (int k = 0; k < PZ; ++k) z[k] = fmaf((float)(k0 + k), p.h, p.oz);
+    for (int k = 0; k < PZ; ++k) z[k] = REL ? (float)(k0 + k) : fmaf((float)(k0 + k), p.h, p.oz);
+    // difference of point coordinate (or index) u and the tile's atom
+    // coordinate a (or origin - atom)
+    auto diff = [&](float u, float a) { return REL ? fmaf(u, p.h, a) : u - a; };
 
     if (tid == 0) {
         for (int s = 0; s < kDirectStages; ++s) mbar_init(&full[s], 1);
@@ -181,7 +192,20 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
         const int stage = it % kDirectStages;
         mbar_wait(&full[stage], (uint32_t)((it / kDirectStages) & 1), p.status);
         const int n = min(kDirectTile, n_local - it * kDirectTile);
-        const float4 *tile = ring + stage * kDirectTile;
+        float4 *tile = ring + stage * kDirectTile;
+        if (REL) {
+            // Once per tile and CTA, each atom becomes (origin - atom, q) in
+            // place, so that every thread forms its differences with one
+            // fused multiply-add each.  These plain stores precede the bulk
+            // copy that later refills the stage, hence the proxy fence
+            // before the barrier.
+            for (int a = tid; a < n; a += kDirectThreads) {
+                const float4 v = tile[a];
+                tile[a] = make_float4(p.ox - v.x, p.oy - v.y, p.oz - v.z, v.w);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncthreads();
+        }
 
         float2 part[NP];
 #pragma unroll
@@ -196,7 +220,7 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
             const float4 at = tile[a];  // same address in the lanes of a slice: broadcast
             float2 dxp[HX];
 #pragma unroll
-            for (int hh = 0; hh < HX; ++hh) dxp[hh] = make_float2(x[2 * hh] - at.x, x[2 * hh + 1] - at.x);
+            for (int hh = 0; hh < HX; ++hh) dxp[hh] = make_float2(diff(x[2 * hh], at.x), diff(x[2 * hh + 1], at.x));
             const float2 q2 = make_float2(at.w, at.w);
             // dy^2 + dz^2 per row: the square of the shorter axis is taken
             // once and the other axis fused into it (PY + PZ*PY operations
@@ -204,12 +228,12 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const __grid_con
             float dy[PY], dy2[PY];
 #pragma unroll
             for (int j = 0; j < PY; ++j) {
-                dy[j] = y[j] - at.y;
+                dy[j] = diff(y[j], at.y);
                 dy2[j] = dy[j] * dy[j];
             }
 #pragma unroll
             for (int k = 0; k < PZ; ++k) {
-                const float dz = z[k] - at.z;
+                const float dz = diff(z[k], at.z);
                 const float dz2 = dz * dz;
 #pragma unroll
                 for (int j = 0; j < PY; ++j) {
@@ -332,12 +356,13 @@ using KernelFn = void (*)(DirectParams);
 struct Variant {
     int px, py, pz, emu, ls;
     double rate;
-    KernelFn vec, scalar;
+    KernelFn fn[2][2];  // [vector stores][relative differences]
 };
 
-#define CP_VARIANT(PX, PY, PZ, EMU, LS, RATE)                                                       \
-    {PX, PY, PZ, EMU, LS, RATE, direct_kernel<PX, PY, PZ, EMU, LS, true>,                           \
-     direct_kernel<PX, PY, PZ, EMU, LS, false>}
+#define CP_VARIANT(PX, PY, PZ, EMU, LS, RATE)                                                              \
+    {PX, PY, PZ, EMU, LS, RATE,                                                                            \
+     {{direct_kernel<PX, PY, PZ, EMU, LS, false, false>, direct_kernel<PX, PY, PZ, EMU, LS, false, true>}, \
+      {direct_kernel<PX, PY, PZ, EMU, LS, true, false>, direct_kernel<PX, PY, PZ, EMU, LS, true, true>}}}
 const Variant kVariants[] = {
     CP_VARIANT(4, 4, 2, 0, 1, 15.48), CP_VARIANT(4, 2, 2, 0, 1, 15.47), CP_VARIANT(4, 4, 1, 0, 1, 15.41),
     CP_VARIANT(4, 2, 1, 0, 1, 15.58), CP_VARIANT(4, 1, 1, 0, 1, 15.31), CP_VARIANT(4, 4, 2, 4, 1, 18.96),
@@ -355,14 +380,14 @@ constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 // sizes above 8 it also sets the non-portable cluster attribute of that
 // exact kernel, which the launch needs.
 std::mutex g_plan_mutex;
-int g_slots[kMaxDevices][kNumVariants][2][kMaxSplit + 1];  // [device][variant][vector stores][split]
+int g_slots[kMaxDevices][kNumVariants][2][2][kMaxSplit + 1];  // [device][variant][vector][relative][split]
 
-int resident_ctas(int v, int s, bool vec, const DeviceInfo &dev) {
+int resident_ctas(int v, int s, bool vec, bool rel, const DeviceInfo &dev) {
     std::lock_guard<std::mutex> lock(g_plan_mutex);
-    int &cached = g_slots[dev.device][v][vec ? 1 : 0][s];
+    int &cached = g_slots[dev.device][v][vec ? 1 : 0][rel ? 1 : 0][s];
     if (cached > 0) return cached;
     if (cached == -2) return 0;  // cluster size not available
-    KernelFn fn = vec ? kVariants[v].vec : kVariants[v].scalar;
+    KernelFn fn = kVariants[v].fn[vec ? 1 : 0][rel ? 1 : 0];
     int slots = 0;
     if (s > kPortableSplit &&
         cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
@@ -431,7 +456,7 @@ bool vector_stores(int v, const Grid &g, int v_align) {
 // CTAs spread evenly over the SMs; the busiest SM runs ceil(CTAs / SMs) of
 // them, at most `resident` at a time, at the shape's measured pair rate
 // scaled by its occupancy; each split level adds a small reduction cost.
-int plan_direct(const Grid &g, int n_atoms, int v_align, const DeviceInfo &dev, Plan *out) {
+int plan_direct(const Grid &g, int n_atoms, int v_align, bool rel, const DeviceInfo &dev, Plan *out) {
     double best = INFINITY;
     for (int v = 0; v < kNumVariants; ++v) {
         const int px = kVariants[v].px, py = kVariants[v].py, pz = kVariants[v].pz;
@@ -447,7 +472,7 @@ int plan_direct(const Grid &g, int n_atoms, int v_align, const DeviceInfo &dev, 
             if (s == 5 || s == 7 || (s > 8 && s != 12 && s != 16)) continue;
             if (s > 1 && (long long)n_atoms < (long long)s * 64) break;
             if (ctas * s > 0x7fffffffll) break;
-            const int slots = resident_ctas(v, s, vec, dev);
+            const int slots = resident_ctas(v, s, vec, rel, dev);
             if (slots < 0) return CP_ERR_CUDA;
             if (slots == 0) continue;  // cluster size not available on this device
             const double resident = std::max(1.0, (double)slots / dev.sm_count);
@@ -479,8 +504,9 @@ int launch_direct(const float *atoms, int n_atoms, const Grid &g, float *V, cuda
     int rc = device_info(&dev);
     if (rc) return rc;
     const int v_align = aligned(V, 16) ? 16 : aligned(V, 8) ? 8 : 4;
+    const bool rel = !grid_points_exact(g);
     Plan plan;
-    rc = plan_direct(g, n_atoms, v_align, dev, &plan);
+    rc = plan_direct(g, n_atoms, v_align, rel, dev, &plan);
     if (rc) return rc;
     if (force_variant >= 0 && force_variant < kNumVariants) {
         const int v = force_variant;
@@ -495,7 +521,7 @@ int launch_direct(const float *atoms, int n_atoms, const Grid &g, float *V, cuda
     }
     if (force_split >= 1 && force_split <= kMaxSplit) plan.split = force_split;
     if (plan.split > kPortableSplit) {  // sets the non-portable cluster attribute, checks support
-        const int slots = resident_ctas(plan.variant, plan.split, plan.vec, dev);
+        const int slots = resident_ctas(plan.variant, plan.split, plan.vec, rel, dev);
         if (slots < 0) return CP_ERR_CUDA;
         if (slots == 0) return CP_ERR_UNSUPPORTED;
     }
@@ -518,7 +544,7 @@ int launch_direct(const float *atoms, int n_atoms, const Grid &g, float *V, cuda
     p.status = device_status_ptr();
     if (!p.status) return CP_ERR_CUDA;
 
-    KernelFn fn = plan.vec ? kVariants[plan.variant].vec : kVariants[plan.variant].scalar;
+    KernelFn fn = kVariants[plan.variant].fn[plan.vec ? 1 : 0][rel ? 1 : 0];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(plan.ptiles * plan.split), 1, 1);
     cfg.blockDim = dim3(kDirectThreads, 1, 1);
@@ -563,11 +589,18 @@ CP_API int cp_direct_plan(int n_atoms, int nx, int ny, int nz, int *variant, int
     rc = device_info(&dev);
     if (rc) return rc;
     Plan plan;
-    rc = plan_direct(g, n_atoms, 16, dev, &plan);
+    rc = plan_direct(g, n_atoms, 16, !grid_points_exact(g), dev, &plan);
     if (rc) return rc;
     *variant = plan.variant;
     *split = plan.split;
     return CP_OK;
+}
+
+CP_API int cp_grid_points_exact(int nx, int ny, int nz, cp_vec3 origin, float h) {
+    Grid g;
+    const int rc = check_grid(nx, ny, nz, origin, h, &g);
+    if (rc) return rc;
+    return grid_points_exact(g) ? 1 : 0;
 }
 
 // Same as cp_direct with the patch shape (index into the variant table

@@ -36,6 +36,36 @@ int check_grid(int nx, int ny, int nz, cp_vec3 origin, float h, Grid *g) {
     return CP_OK;
 }
 
+namespace {
+
+// Exponent of the lowest set bit of a nonzero finite float: f is an odd
+// integer times 2^low_bit(f).
+int low_bit(float f) {
+    int e = 0;
+    const double m = std::frexp(std::fabs((double)f), &e);  // f = m 2^e, m in [0.5, 1)
+    unsigned long long mant = (unsigned long long)std::ldexp(m, 53);  // exact: 53-bit integer
+    int tz = 0;
+    while ((mant & 1ull) == 0ull) {
+        mant >>= 1;
+        ++tz;
+    }
+    return e - 53 + tz;
+}
+
+bool axis_exact(float o, float h, int n) {
+    int q = low_bit(h);
+    if (o != 0.0f) q = std::min(q, low_bit(o));
+    const double lim = std::ldexp(1.0, 24 + q);
+    const double a = std::fabs((double)o), b = std::fabs((double)o + (double)(n - 1) * (double)h);
+    return q >= -126 && a < lim && b < lim;  // no subnormal steps either
+}
+
+}  // namespace
+
+bool grid_points_exact(const Grid &g) {
+    return axis_exact(g.ox, g.h, g.nx) && axis_exact(g.oy, g.h, g.ny) && axis_exact(g.oz, g.h, g.nz);
+}
+
 int check_cutoff_args(const Grid &, float cutoff, float bin_size, int capacity) {
     if (!std::isfinite(cutoff) || !(cutoff > 0.0f)) return CP_ERR_INVALID_ARGUMENT;
     if (!std::isfinite(bin_size) || !(bin_size > 0.0f)) return CP_ERR_INVALID_ARGUMENT;

@@ -25,6 +25,13 @@ struct Grid {
     long long npoints;
 };
 
+// True when every grid coordinate origin_d + i*h (0 <= i < n_d) is exactly
+// representable in fp32, so that forming a point and subtracting an atom
+// rounds only once.  Sufficient, not necessary: o + i*h are all multiples of
+// 2^q, q the lowest set bit of o or h, and such a multiple is exact in fp32
+// when its magnitude is below 2^(24 + q).
+bool grid_points_exact(const Grid &g);
+
 // Bin grid of the cutoff map (see cpmap.h for the definitions).
 struct BinGeom {
     int nb[3];

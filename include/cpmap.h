@@ -123,10 +123,22 @@ CP_API int cp_direct_config(const float *atoms, int n_atoms, int nx, int ny, int
 
 /* The patch shape (variant index as for cp_direct_config) and cluster split
  * that cp_direct would use for this grid and atom count on the current
- * device (assuming 16-byte aligned output).  Queries occupancy, launches
- * nothing.  Returns CP_OK, CP_ERR_INVALID_ARGUMENT, CP_ERR_TOO_LARGE or
+ * device (assuming 16-byte aligned output and grid points exact in fp32,
+ * e.g. origin 0 and h 1).  Queries occupancy, launches nothing.  Returns CP_OK, CP_ERR_INVALID_ARGUMENT, CP_ERR_TOO_LARGE or
  * CP_ERR_CUDA.                                                              */
 CP_API int cp_direct_plan(int n_atoms, int nx, int ny, int nz, int *variant, int *split);
+
+/* Whether every grid coordinate origin_d + i*h (0 <= i < n_d, each axis) is
+ * exactly representable in fp32: 1 if so, 0 if not (or not provably), or a
+ * negative cp_status for an invalid grid.  Host only.  The direct and
+ * cutoff kernels use it to choose how they form a point-atom difference:
+ * for exact points as point - atom, rounded once; otherwise as
+ * i*h + (origin - atom) with one fused multiply-add, so that the rounding
+ * follows the atom's offset from the grid origin rather than the grid's
+ * distance from the coordinate origin.  The test is sufficient: all o + i*h
+ * are multiples of 2^q, q the lowest set bit of o or h, and are exact when
+ * both ends of the axis are below 2^(24 + q) in magnitude.                  */
+CP_API int cp_grid_points_exact(int nx, int ny, int nz, cp_vec3 origin, float h);
 
 /* ------------------------------------------------------------------------ */
 /* Cutoff summation (Input Binning lecture, slides 24-37).

@@ -261,3 +261,40 @@ def test_msm_rejects_on_host():
     assert call(12.0, 2.0, atoms=FAKE_MIS) == -2
     assert lib.cp_atom_bounds(FAKE, 0, FAKE, None) == -1
     assert lib.cp_atom_bounds(FAKE_MIS, 5, FAKE, None) == -2
+
+
+def _axis_exact_brute(o, h, n):
+    o64, h64 = float(np.float32(o)), float(np.float32(h))
+    v = o64 + np.arange(n, dtype=np.float64) * h64
+    return bool(np.all(v.astype(np.float32).astype(np.float64) == v))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_grid_points_exact_is_sound(seed):
+    """cp_grid_points_exact (which picks the kernels' difference form) never
+    claims exact fp32 grid points that are not, checked point by point; it
+    recognises the dyadic benchmark grids; and it rejects an invalid grid."""
+    lib = cp.library()
+    rng = np.random.default_rng(seed)
+    hs = [0.5, 0.25, 0.37, 0.1, 1.0, 0.3, 0.125, 2.0 ** -10]
+    for _ in range(60):
+        n = [int(v) for v in rng.integers(1, 400, size=3)]
+        h = float(np.float32(hs[rng.integers(len(hs))]))
+        kind = rng.integers(3)
+        scale = [1.0, 100.0, 1e5][rng.integers(3)]
+        if kind == 0:
+            o = [float(np.float32(np.round(v * 4) / 4)) for v in rng.uniform(-scale, scale, 3)]
+        elif kind == 1:
+            o = [float(np.float32(v)) for v in rng.uniform(-scale, scale, 3)]
+        else:
+            o = [0.0, 0.0, float(np.float32(10 * h))]
+        got = lib.cp_grid_points_exact(*n, _lib.cp_vec3(*o), h)
+        assert got in (0, 1)
+        brute = all(_axis_exact_brute(o[d], h, n[d]) for d in range(3))
+        if got == 1:
+            assert brute, (n, o, h)
+    for shape, origin in [((128, 128, 64), (0, 0, 0)), ((200, 200, 200), (0, 0, 0)), ((100, 100, 1), (0, 0, 5.0)),
+                          ((400, 400, 400), (0, 0, 0))]:
+        assert lib.cp_grid_points_exact(*shape, _lib.cp_vec3(*origin), 0.5) == 1
+    assert lib.cp_grid_points_exact(20, 14, 11, _lib.cp_vec3(5000.1234567, -4999.2345679, 2500.31415), 0.37) == 0
+    assert lib.cp_grid_points_exact(0, 4, 4, _lib.cp_vec3(0, 0, 0), 0.5) == -1

@@ -166,3 +166,28 @@ def test_degenerate_grids(shape):
         torch.cuda.synchronize()
         assert_within_bound(Vc.cpu().numpy(), refc, boundc, f"{shape} cutoff K={K}")
     assert cp.device_status() == 0
+
+
+@pytest.mark.parametrize("offset", [0.0, 200.0, 5000.0])
+def test_grids_far_from_the_coordinate_origin(offset):
+    """Differences are formed as index * h + (origin - atom), rounded once, so the
+    accuracy does not depend on where the grid sits: a grid 5000 A from the
+    coordinate origin with h = 0.37 A (grid points not exact in fp32) meets the
+    same bound at every point.  Forming the point first and subtracting the atom
+    after would carry ulp(5000)/2 = 2.4e-4 A into every difference, above the
+    bound for atoms 0.1 A from a point."""
+    origin = (offset + 0.1234567, -offset + 0.7654321, offset / 2 + 0.31415)
+    w = workloads.random_case(95, 1200, (20, 14, 11), h=0.37, origin=origin, margin=2.5)
+    a = to_dev(w.atoms)
+    ref, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+    for v, split in ((-1, 0), (7, 1), (18, 3), (10, 1)):
+        V = cp.direct(a, w.shape, w.origin, w.h, variant=v, split=split)
+        torch.cuda.synchronize()
+        assert_within_bound(V.cpu().numpy(), ref, bound, f"offset {offset} variant {v}")
+    c, b = 2.0, 0.9
+    refc, boundc = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, c)
+    for K in (0, 16):
+        Vc = cp.cutoff(a, w.shape, w.origin, w.h, c, b, capacity=K)
+        torch.cuda.synchronize()
+        assert_within_bound(Vc.cpu().numpy(), refc, boundc, f"offset {offset} cutoff K={K}")
+    assert cp.device_status() == 0
