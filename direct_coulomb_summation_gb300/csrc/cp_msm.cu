@@ -466,7 +466,11 @@ __global__ void __launch_bounds__(kMsmThreads) msm_reduce_prolong_kernel(const _
 
 struct InterpParams {
     int nx, ny, nz;
-    float ox, oy, oz, h;
+    // grid origin minus lattice origin (rounded once on the host): a point's
+    // offset from the lattice origin is i*h + this, formed with one fused
+    // multiply-add, so its rounding follows the offset, not the distance of
+    // the grid from the coordinate origin
+    float dox, doy, doz, h;
     long long quads;
     int qx;
     float *V;
@@ -483,8 +487,8 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_kernel(const __grid_co
     const int k = (int)(quad / ((long long)g.qx * g.ny));
     const int i0 = 4 * qx;
     const MsmLevelDev &L0 = p.lv[0];
-    const float ty = msm_t(fmaf((float)j, g.h, g.oy), p.o[1], p.h0);
-    const float tz = msm_t(fmaf((float)k, g.h, g.oz), p.o[2], p.h0);
+    const float ty = __fdiv_rn(fmaf((float)j, g.h, g.doy), p.h0);
+    const float tz = __fdiv_rn(fmaf((float)k, g.h, g.doz), p.h0);
     const int ky = (int)floorf(ty), kz = (int)floorf(tz);
     float wy[4], wz[4];
 #pragma unroll
@@ -496,7 +500,7 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_kernel(const __grid_co
     int kx[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        tx[c] = msm_t(fmaf((float)min(i0 + c, g.nx - 1), g.h, g.ox), p.o[0], p.h0);
+        tx[c] = __fdiv_rn(fmaf((float)min(i0 + c, g.nx - 1), g.h, g.dox), p.h0);
         kx[c] = (int)floorf(tx[c]);
     }
     // node (i, j, k) of level 0 at e[(k - lo z) ...]
@@ -594,14 +598,14 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_brick_kernel(const __g
         const int d = tid / kBrick, pt = tid % kBrick;
         const int n = d == 0 ? g.nx : (d == 1 ? g.ny : g.nz);
         const int b = d == 0 ? bx : (d == 1 ? by : bz);
-        const float o = d == 0 ? g.ox : (d == 1 ? g.oy : g.oz);
+        const float o = d == 0 ? g.dox : (d == 1 ? g.doy : g.doz);
         const int idx = min(kBrick * b + pt, n - 1);  // points past the edge repeat the last one
         // lattice coordinate of the point: weights only, so a reciprocal
         // multiply suffices (the cell sort's exact division is for atoms)
         const float inv_h0 = 1.0f / p.h0;
-        const float t = (fmaf((float)idx, g.h, o) - p.o[d]) * inv_h0;
+        const float t = fmaf((float)idx, g.h, o) * inv_h0;
         const int k = min(max((int)floorf(t), 0), p.cells[d] - 1);
-        const float t0 = (fmaf((float)(kBrick * b), g.h, o) - p.o[d]) * inv_h0;
+        const float t0 = fmaf((float)(kBrick * b), g.h, o) * inv_h0;
         const int k0 = min(max((int)floorf(t0), 0), p.cells[d] - 1);
         off[d][pt] = k - k0;
         for (int a = 0; a < 4; ++a) wgt[d][pt][a] = msm_phi(t - (float)(k - 1 + a));
@@ -979,9 +983,9 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     ip.nx = g.nx;
     ip.ny = g.ny;
     ip.nz = g.nz;
-    ip.ox = g.ox;
-    ip.oy = g.oy;
-    ip.oz = g.oz;
+    ip.dox = (float)((double)g.ox - (double)p.o[0]);
+    ip.doy = (float)((double)g.oy - (double)p.o[1]);
+    ip.doz = (float)((double)g.oz - (double)p.o[2]);
     ip.h = g.h;
     ip.qx = (g.nx + 3) / 4;
     ip.quads = (long long)ip.qx * g.ny * g.nz;

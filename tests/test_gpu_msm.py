@@ -63,6 +63,15 @@ CASES = [
     # grid spacing above the lattice spacing: the per-quad interpolation kernel
     ("grid_coarser_than_lattice", workloads.random_case(706, 600, (21, 14, 11), h=1.0, origin=(0.5, -1.0, 2.0),
                                                         margin=3.0, cutoff=3.0, bin_size=1.5), 0.7),
+    # 5000 A from the coordinate origin with grid points that are not fp32
+    # numbers: point lattice coordinates are formed from the grid origin's
+    # offset to the lattice origin, so their rounding does not grow with 5000 A
+    ("far_origin", workloads.random_case(708, 500, (20, 14, 11), h=0.37,
+                                         origin=(5000.1234567, -4999.2345679, 2500.31415), margin=3.0,
+                                         cutoff=3.0, bin_size=1.5), 0.7),
+    ("far_origin_coarse_grid", workloads.random_case(709, 500, (15, 12, 9), h=1.03,
+                                                     origin=(-5000.4321, 3000.777, 4999.9), margin=3.0,
+                                                     cutoff=3.0, bin_size=1.5), 0.7),
 ]
 
 
