@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_brick_kernel(const __g
         v[c] = s;
     }
     const int i0 = kBrick * bx + 4 * half, j = kBrick * by + py, k = kBrick * bz + pz;
-    if (j >= g.ny || k >= g.nz) return;
+    if (i0 >= g.nx || j >= g.ny || k >= g.nz) return;  // half-rows past the grid store nothing
     if (!CP_IN(((long long)k * g.ny + j) * g.nx + i0, (long long)g.nx * g.ny * g.nz, p.status)) return;
     float *row = g.V + ((long long)k * g.ny + j) * g.nx;
     if (i0 + 3 < g.nx && (g.nx % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.V) & 15) == 0)) {

@@ -5,8 +5,9 @@ child process with CPMAP_CHECKED=1 runs the direct map (every patch shape,
 cluster splits 1, 8 and 16, an odd nx), the cutoff map with capacity 0, 8
 and 16 (a ragged grid, a crowded bin, the 200^3 benchmark map), the binning
 stage and the long-range part (both interpolation kernels, one and four
-levels); the device status must stay clean and the maps must equal the
-release build's bit for bit."""
+levels), and a grid 5000 A from the coordinate origin whose points are not
+fp32 numbers (the kernels' relative-difference paths); the device status
+must stay clean and the maps must equal the release build's bit for bit."""
 import os
 import subprocess
 import sys
@@ -62,6 +63,20 @@ SCRIPT = textwrap.dedent('''
         at = torch.from_numpy(t.atoms).cuda()
         out["msm_top"] = cp.msm_longrange(at, t.shape, t.origin, t.h, t.cutoff, 1.0,
                                           domain=((0.0, 0.0, 0.0), (4.0, 4.0, 4.0)))
+        # grid points that are not fp32 numbers: the kernels' relative differences
+        f = workloads.random_case(905, 900, (20, 14, 11), h=0.37, origin=(5000.1234567, -4999.2345679, 2500.31415),
+                                  margin=3.0, cutoff=3.0, bin_size=1.5)
+        af = torch.from_numpy(f.atoms).cuda()
+        for v in (4, 7, 12, 16, 18):
+            for s in (1, 8):
+                out[f"far_direct_{v}_{s}"] = cp.direct(af, f.shape, f.origin, f.h, variant=v, split=s)
+        for K in (0, 16):
+            out[f"far_cutoff_{K}"] = cp.cutoff(af, f.shape, f.origin, f.h, f.cutoff, f.bin_size, K)
+        out["far_msm"] = cp.msm_longrange(af, f.shape, f.origin, f.h, f.cutoff, 0.7, domain=cp.atom_bounds(af))
+        # nx = 20: the last brick's second half-row of the interpolation lies past the grid
+        for h0 in (0.4, 0.7, 1.0):
+            out[f"far_msm_{h0}"] = cp.msm_longrange(af, f.shape, f.origin, f.h, f.cutoff, h0,
+                                                    domain=cp.atom_bounds(af))
         torch.cuda.synchronize()
         return {k: v.cpu().numpy() for k, v in out.items()}
 
