@@ -191,3 +191,41 @@ def test_grids_far_from_the_coordinate_origin(offset):
         torch.cuda.synchronize()
         assert_within_bound(Vc.cpu().numpy(), refc, boundc, f"offset {offset} cutoff K={K}")
     assert cp.device_status() == 0
+
+
+def test_random_geometries():
+    """60 seeded random geometries: grid shape 1..39 per axis, spacing 0.2..1.5 A
+    (dyadic or not), origin near or 1000..5000 A from the coordinate origin,
+    1..2500 atoms, cutoff 1..6 A, bin 0.5..3 A, a random capacity, patch shape and
+    cluster split.  Direct (planner and forced) and cutoff maps against the oracle
+    at every point, a clean device status after each call.  Calls the library
+    rejects on the host (offset lists beyond its limit) are skipped."""
+    rng = np.random.default_rng(606)
+    for it in range(60):
+        shape = tuple(int(v) for v in rng.integers(1, 40, size=3))
+        h = float(np.float32(rng.choice([0.5, 0.25, 1.0]) if rng.random() < 0.4 else rng.uniform(0.2, 1.5)))
+        shift = rng.uniform(1e3, 5e3, 3) * rng.choice([-1, 1], 3) if rng.random() < 0.3 else np.zeros(3)
+        origin = tuple(float(np.float32(v)) for v in rng.uniform(-50, 50, 3) + shift)
+        n = int(rng.integers(1, 2500))
+        c = float(np.float32(rng.uniform(1.0, 6.0)))
+        b = float(np.float32(rng.uniform(0.5, 3.0)))
+        w = workloads.random_case(20_000 + it, n, shape, h=h, origin=origin, margin=float(rng.uniform(0.0, c + 2.0)))
+        a = to_dev(w.atoms)
+        tag = f"case {it}: shape {shape} h {h:.4g} origin {origin} n {n} c {c:.3g} b {b:.3g}"
+        ref, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+        v, s = int(rng.integers(0, len(cp.DIRECT_VARIANTS))), int(rng.choice([1, 2, 3, 4, 6, 8]))
+        for kw in ({}, {"variant": v, "split": s}):
+            V = cp.direct(a, w.shape, w.origin, w.h, **kw)
+            torch.cuda.synchronize()
+            assert_within_bound(V.cpu().numpy(), ref, bound, f"{tag} direct {kw}")
+            assert cp.device_status() == 0, tag
+        K = int(rng.choice([0, 8, 16]))
+        try:
+            Vc = cp.cutoff(a, w.shape, w.origin, w.h, c, b, capacity=K)
+        except cp.CpError as e:
+            assert e.code == -3, tag  # CP_ERR_TOO_LARGE: offset list beyond the library's limit
+            continue
+        torch.cuda.synchronize()
+        refc, boundc = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, c)
+        assert_within_bound(Vc.cpu().numpy(), refc, boundc, f"{tag} cutoff K={K}")
+        assert cp.device_status() == 0, tag
