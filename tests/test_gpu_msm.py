@@ -243,3 +243,35 @@ def test_public_api_with_host_arrays():
     auto = cp.msm_longrange(a, w.shape, w.origin, w.h, w.cutoff, h0)
     torch.cuda.synchronize()
     assert torch.equal(auto, dev_long)
+
+
+def test_longrange_random_geometries():
+    """20 seeded random geometries: grid shape 1..29 per axis, spacing 0.2..1.5 A
+    (dyadic or not), origin near or 1000..5000 A from the coordinate origin,
+    1..1500 atoms, c = 1.5..5 A, h0 = 0.35..1.6 A (one or more levels, both
+    interpolation kernels), against the oracle at every point within 1e-5 B(x).
+    Calls the library rejects on the host (a stencil beyond its radius limit)
+    are skipped."""
+    rng = np.random.default_rng(5)
+    for it in range(20):
+        shape = tuple(int(v) for v in rng.integers(1, 30, size=3))
+        h = float(np.float32(rng.choice([0.5, 0.25, 1.0]) if rng.random() < 0.4 else rng.uniform(0.2, 1.5)))
+        shift = rng.uniform(1e3, 5e3, 3) * rng.choice([-1, 1], 3) if rng.random() < 0.3 else np.zeros(3)
+        origin = tuple(float(np.float32(v)) for v in rng.uniform(-30, 30, 3) + shift)
+        n = int(rng.integers(1, 1500))
+        c = float(np.float32(rng.uniform(1.5, 5.0)))
+        h0 = float(np.float32(rng.uniform(0.35, 1.6)))
+        w = workloads.random_case(30_000 + it, n, shape, h=h, origin=origin, margin=float(rng.uniform(0.0, c + 2.0)))
+        a = torch.from_numpy(w.atoms).cuda()
+        dom = cp.atom_bounds(a)
+        try:
+            V = cp.msm_longrange(a, w.shape, w.origin, w.h, c, h0, domain=dom)
+        except cp.CpError as e:
+            assert e.code == -3, e  # CP_ERR_TOO_LARGE
+            continue
+        torch.cuda.synchronize()
+        assert cp.device_status() == 0
+        got = V.cpu().numpy().reshape(-1).astype(np.float64)
+        ref = msm.long_range(w.atoms, w.shape, w.origin, w.h, dom[0], dom[1], c, h0)
+        B = msm.abs_charge_bound(w.atoms, w.shape, w.origin, w.h, c)
+        _check(got, ref, B, 1e-5, f"case {it}: shape {shape} h {h:.4g} origin {origin} c {c:.3g} h0 {h0:.3g}")
