@@ -92,8 +92,12 @@ typedef struct {
 /* Direct Coulomb summation (notes, sections 18.1-18.4).
  *
  * V(g) = sum over all n_atoms atoms of q / r for every grid point, computed
- * in fp32 with rsqrt on the SFU, atom tiles accumulated block-wise.
- * n_atoms may be 0 (V is then all zero).  Needs no workspace.
+ * in fp32 (rsqrt on the SFU for most pairs, on the FMA pipe for a fixed
+ * share), atom tiles accumulated block-wise.  Point-atom differences are
+ * rounded once wherever the grid sits (see cp_grid_points_exact).
+ * n_atoms may be 0 (V is then all zero).  Atoms are used as given: one
+ * with a non-finite coordinate or charge makes every value non-finite (the
+ * cutoff map drops such atoms instead).  Needs no workspace.
  * Returns CP_OK, CP_ERR_INVALID_ARGUMENT, CP_ERR_MISALIGNED (atoms not
  * 16-byte aligned), CP_ERR_TOO_LARGE or CP_ERR_CUDA.                        */
 CP_API int cp_direct(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float *V,
