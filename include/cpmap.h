@@ -95,9 +95,11 @@ typedef struct {
  * in fp32 (rsqrt on the SFU for most pairs, on the FMA pipe for a fixed
  * share), atom tiles accumulated block-wise.  Point-atom differences are
  * rounded once wherever the grid sits (see cp_grid_points_exact).
- * n_atoms may be 0 (V is then all zero).  Atoms are used as given: one
- * with a non-finite coordinate or charge makes every value non-finite (the
- * cutoff map drops such atoms instead).  Needs no workspace.
+ * n_atoms may be 0 (V is then all zero).  Atoms are used as given and
+ * must be finite and within 1e18 A of the grid, so that r^2 fits fp32
+ * (farther atoms contribute about q/r, i.e. nothing measurable, up to that
+ * limit; beyond it the FMA-pipe route overflows to inf).  The cutoff map
+ * drops non-finite and out-of-range atoms instead.  Needs no workspace.
  * Returns CP_OK, CP_ERR_INVALID_ARGUMENT, CP_ERR_MISALIGNED (atoms not
  * 16-byte aligned), CP_ERR_TOO_LARGE or CP_ERR_CUDA.                        */
 CP_API int cp_direct(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float *V,

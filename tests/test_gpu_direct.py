@@ -152,3 +152,18 @@ def test_direct_superposition_on_gpu():
     bound = torch.from_numpy(bound).cuda().reshape(vab.shape)
     assert torch.all((vab - va - vb).abs() <= 2e-4 * bound)
     assert torch.equal(vn, -vab.float())  # exact: each term negates
+
+
+def test_direct_far_atoms():
+    """Atoms 1e17 A away (padding a caller might use; the documented limit is
+    1e18 A, where r^2 still fits fp32) contribute nothing measurable, on both
+    rsqrt routes and with grid points that are or are not fp32 numbers."""
+    pad = np.array([[1e17, 0, 0, 1.0], [0, -1e17, 5, -0.5], [3e16, 2e16, -5e16, 0.7]], dtype=np.float32)
+    for h, origin in ((0.5, (0.0, 0.0, 0.0)), (0.37, (1.2345, -0.5432, 2.111))):
+        w = workloads.random_case(12, 900, (24, 16, 8), h=h, origin=origin, margin=1.0)
+        atoms = np.concatenate([w.atoms, pad])
+        ref, bound = oracle.direct(w.atoms, w.shape, w.origin, w.h)
+        for v in (-1, 7, 17, 18):
+            V = cp.direct(to_dev(atoms), w.shape, w.origin, w.h, variant=v)
+            torch.cuda.synchronize()
+            assert_within_bound(V.cpu().numpy(), ref, bound, f"h {h} variant {v}")
