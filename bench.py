@@ -488,7 +488,12 @@ def run_ours(args):
     t_direct = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
     t_bin = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
     t_map = sum(e[3].elapsed_time(e[4]) for e in ev) / 1e3
-    t_direct, t_bin, t_map, t_wall = max_over_ranks([t_direct, t_bin, t_map, t_wall], device)
+    # medians of the per-step leg times (ms), beside the means that the rates use
+    med_direct = float(np.median([e[0].elapsed_time(e[1]) for e in ev]))
+    med_cut = float(np.median([e[2].elapsed_time(e[4]) for e in ev]))
+    med_map = float(np.median([e[3].elapsed_time(e[4]) for e in ev]))
+    t_direct, t_bin, t_map, t_wall, med_direct, med_cut, med_map = max_over_ranks(
+        [t_direct, t_bin, t_map, t_wall, med_direct, med_cut, med_map], device)
     t_direct, t_bin, t_map = (max(t, 1e-12) for t in (t_direct, t_bin, t_map))
     K = args.steps
     direct_pairs = float(wd.n_pairs) * world * K
@@ -602,6 +607,7 @@ def run_ours(args):
             "pair_evals_per_s": direct_rate,
             "grid_points_per_s": float(wd.n_points) * world * K / t_direct,
             "ms": 1e3 * t_direct / K,
+            "ms_median": med_direct if do_direct else None,
         },
         "cutoff": {
             "grid_points_per_s": points_rate,
@@ -610,8 +616,10 @@ def run_ours(args):
             "examined_pairs_per_s": counts["examined"] * world * K / t_cut,
             "pairs_per_step": counts,
             "ms": 1e3 * t_cut / K,
+            "ms_median": med_cut if do_cutoff else None,
             "ms_binning": 1e3 * t_bin / K,
             "ms_map": 1e3 * t_map / K,
+            "ms_map_median": med_map if do_cutoff else None,
             "ms_as_cuda_graph": None if t_graph_cut is None else 1e3 * t_graph_cut,
             "roofline_map": {
                 "bound": "alu", "kernel": "cutoff_brick_kernel (cp_cutoff_map)",
