@@ -723,6 +723,15 @@ def run_compare(args):
         res[f"gpu {name}"] = {"ms": mean, "ms_median": med}
     mean, med = timed(lambda: cp.direct(a, w.shape, w.origin, w.h, out=V))
     res["gpu cp_direct (this library)"] = {"ms": mean, "ms_median": med}
+    # the same call captured once as a CUDA graph and replayed: on a map this
+    # small, the difference is the per-launch host and launch overhead
+    graph = torch.cuda.CUDAGraph()
+    cp.direct(a, w.shape, w.origin, w.h, out=V)  # plans and sets kernel attributes before capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        cp.direct(a, w.shape, w.origin, w.h, out=V)
+    mean, med = timed(graph.replay)
+    res["gpu cp_direct (this library), replayed as a CUDA graph"] = {"ms": mean, "ms_median": med}
     for v in res.values():
         v["pair_evals_per_s"] = w.n_pairs / (v["ms"] * 1e-3)
         v["speedup_vs_sequential"] = seq_ms / v["ms"]
