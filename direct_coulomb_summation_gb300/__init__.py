@@ -326,7 +326,7 @@ def device_status(stream=None) -> int:
     return int(bits.value)
 
 
-PIPE_KINDS = {"mufu_rsqrt": 0, "ffma": 1, "mufu_ex2": 2, "ffma2": 3, "ffma2_ffma_mix": 4}
+PIPE_KINDS = {"mufu_rsqrt": 0, "ffma": 1}
 
 
 def eval_rsqrt(x: "torch.Tensor", kind: str = "sfu", stream=None) -> "torch.Tensor":

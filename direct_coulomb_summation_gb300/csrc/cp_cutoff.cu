@@ -682,23 +682,38 @@ struct Prepared {
     BinParams bp;
 };
 
-int prepare(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff,
-            float bin_size, int capacity, void *workspace, size_t workspace_bytes, Prepared *out) {
+// Host-only part of the set-up: arguments, bin geometry and workspace layout.
+int plan(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff,
+         float bin_size, int capacity, Prepared *out) {
     int rc = check_grid(nx, ny, nz, origin, h, &out->g);
     if (rc) return rc;
-    if (n_atoms < 0 || (n_atoms > 0 && !atoms) || !workspace) return CP_ERR_INVALID_ARGUMENT;
+    if (n_atoms < 0 || (n_atoms > 0 && !atoms)) return CP_ERR_INVALID_ARGUMENT;
     rc = check_cutoff_args(out->g, cutoff, bin_size, capacity);
     if (rc) return rc;
     if (n_atoms > 0 && !aligned(atoms, 16)) return CP_ERR_MISALIGNED;
-    if (!aligned(workspace, 256)) return CP_ERR_MISALIGNED;
     rc = make_bin_geometry(out->g, cutoff, bin_size, &out->bg);
     if (rc) return rc;
     rc = make_layout(n_atoms, out->bg, capacity, &out->L);
     if (rc) return rc;
-    if (workspace_bytes < out->L.total_bytes) return CP_ERR_WORKSPACE_TOO_SMALL;
     if ((long long)out->bg.nbins * capacity > INT_MAX) return CP_ERR_TOO_LARGE;
+    return CP_OK;
+}
+
+// Places the planned arrays in `workspace` (layout out->L).
+int bind(const float *atoms, int n_atoms, void *workspace, size_t workspace_bytes, Prepared *out) {
+    if (!workspace) return CP_ERR_INVALID_ARGUMENT;
+    if (!aligned(workspace, 256)) return CP_ERR_MISALIGNED;
+    if (workspace_bytes < out->L.total_bytes) return CP_ERR_WORKSPACE_TOO_SMALL;
     out->bp = bin_params(reinterpret_cast<const float4 *>(atoms), n_atoms, out->bg, out->L, workspace);
     return CP_OK;
+}
+
+int prepare(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff,
+            float bin_size, int capacity, void *workspace, size_t workspace_bytes, Prepared *out) {
+    if (!workspace) return CP_ERR_INVALID_ARGUMENT;
+    int rc = plan(atoms, n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, out);
+    if (rc) return rc;
+    return bind(atoms, n_atoms, workspace, workspace_bytes, out);
 }
 
 int launch_binning(const Prepared &P, cudaStream_t stream) { return launch_binning_params(P.bp, stream); }
@@ -921,18 +936,19 @@ CP_API int cp_cutoff_no_alloc(const float *atoms, int n_atoms, int nx, int ny, i
                               float cutoff, float bin_size, int capacity, float *V, void *stream) {
     if (!V) return CP_ERR_INVALID_ARGUMENT;
     if (!aligned(V, 4)) return CP_ERR_MISALIGNED;
-    cp_cutoff_layout L;
-    int rc = cp_cutoff_layout_of(n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, &L);
+    // One layout, computed once: it decides both the size check and where
+    // the arrays go in the fixed array.
+    Prepared P;
+    int rc = plan(atoms, n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, &P);
     if (rc) return rc;
-    if (L.total_bytes > kStaticWorkspaceBytes) return CP_ERR_TOO_LARGE;  // beyond the fixed 16 MiB
+    if (P.L.total_bytes > kStaticWorkspaceBytes) return CP_ERR_TOO_LARGE;  // beyond the fixed 16 MiB
     void *ws = static_workspace_ptr();
     if (!ws) return CP_ERR_CUDA;
     // Every call reuses the same array and finds the previous call's bins in
     // it.  Nothing carries over: the binning stage zeroes the per-bin counters
     // and the counters block before counting, and every other array is
     // rewritten in full before it is read.
-    Prepared P;
-    rc = prepare(atoms, n_atoms, nx, ny, nz, origin, h, cutoff, bin_size, capacity, ws, kStaticWorkspaceBytes, &P);
+    rc = bind(atoms, n_atoms, ws, kStaticWorkspaceBytes, &P);
     if (rc) return rc;
     static thread_local OffsetList OL;
     rc = make_offset_list(P.g, P.bg, &OL);

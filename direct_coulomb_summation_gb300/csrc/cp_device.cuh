@@ -110,7 +110,11 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 // Waits for phase `parity` of `bar` to complete, at most kWaitLimitNs.  On
 // time-out it sets CP_DEVICE_WAIT_TIMEOUT in *status and returns false; the
 // caller then carries on (its data are wrong, the status says so) so that no
-// thread is left behind at a later block barrier.
+// thread is left behind at a later block barrier.  After a time-out the
+// CTA's shared memory is undefined: a bulk copy issued before it may still
+// land in a stage that is being reused, or after the CTA has exited.  The
+// launch's results are then invalid, which the status word reports; the
+// issuing threads stop issuing copies once one of their waits gave up.
 __device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, unsigned int *status,
                                                 unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -1,6 +1,6 @@
 // cp_probe.cu -- microbenchmarks of the SM pipes the potential map runs on:
-// the SFU (MUFU) reciprocal square root and exponential, and the FP32 FMA
-// pipe (scalar and paired f32x2).  They give the per-SM, per-clock
+// the SFU (MUFU) reciprocal square root and the FP32 FMA pipe.  They give
+// the per-SM, per-clock
 // throughputs that the roofline of the direct and cutoff kernels is built
 // from.  One CTA per SM (a large shared-memory request keeps a second CTA
 // off the SM); each CTA times itself with clock64, so the rate is per SM
@@ -33,34 +33,6 @@ __global__ void probe_kernel(int iters, float seed, long long *cycles, float *si
                 v[c] = sfu_rsqrt(v[c]);
             } else if (KIND == 1) {
                 v[c] = fmaf(v[c], 0.999f, 0.0013f);
-            } else if (KIND == 2) {
-                float y;
-                asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(v[c]));
-                v[c] = y;
-            }
-        }
-        if (KIND == 4) {  // half the chains in f32x2 pairs, half scalar, interleaved
-#pragma unroll
-            for (int c = 0; c < kProbeChains / 2; c += 2) {
-                unsigned long long a, r;
-                asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(v[c]), "f"(v[c + 1]));
-                const unsigned long long m = 0x3f7fbe773f7fbe77ull;  // (0.999f, 0.999f)
-                const unsigned long long d = 0x3aaa64c33aaa64c3ull;  // (0.0013f, 0.0013f)
-                asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(m), "l"(d));
-                asm("mov.b64 {%0, %1}, %2;" : "=f"(v[c]), "=f"(v[c + 1]) : "l"(r));
-                v[kProbeChains / 2 + c] = fmaf(v[kProbeChains / 2 + c], 0.999f, 0.0013f);
-                v[kProbeChains / 2 + c + 1] = fmaf(v[kProbeChains / 2 + c + 1], 0.999f, 0.0013f);
-            }
-        }
-        if (KIND == 3) {
-#pragma unroll
-            for (int c = 0; c < kProbeChains; c += 2) {
-                unsigned long long a, r;
-                asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(v[c]), "f"(v[c + 1]));
-                const unsigned long long m = 0x3f7fbe773f7fbe77ull;  // (0.999f, 0.999f)
-                const unsigned long long d = 0x3aaa64c33aaa64c3ull;  // (0.0013f, 0.0013f)
-                asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(m), "l"(d));
-                asm("mov.b64 {%0, %1}, %2;" : "=f"(v[c]), "=f"(v[c + 1]) : "l"(r));
             }
         }
     }
@@ -119,7 +91,7 @@ CP_API int cp_eval_rsqrt(int kind, const float *x, float *y, int n, void *stream
 }
 
 CP_API int cp_probe_pipe_rate(int kind, int warps, int iters, double *ops_per_clk, double *ms, void *stream) {
-    if (kind < 0 || kind > 4 || warps < 1 || warps > 32 || iters < 1 || !ops_per_clk) return CP_ERR_INVALID_ARGUMENT;
+    if (kind < 0 || kind > 1 || warps < 1 || warps > 32 || iters < 1 || !ops_per_clk) return CP_ERR_INVALID_ARGUMENT;
     DeviceInfo dev;
     int rc = device_info(&dev);
     if (rc) return rc;
@@ -131,8 +103,7 @@ CP_API int cp_probe_pipe_rate(int kind, int warps, int iters, double *ops_per_cl
         cudaFree(cycles);
         return CP_ERR_CUDA;
     }
-    void (*fns[5])(int, float, long long *, float *) = {probe_kernel<0>, probe_kernel<1>, probe_kernel<2>,
-                                                         probe_kernel<3>, probe_kernel<4>};
+    void (*fns[2])(int, float, long long *, float *) = {probe_kernel<0>, probe_kernel<1>};
     auto fn = fns[kind];
     rc = CP_OK;
     cudaEvent_t e0 = nullptr, e1 = nullptr;

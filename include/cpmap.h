@@ -270,7 +270,9 @@ CP_API int cp_cutoff_pair_counts(const float *atoms, int n_atoms, int nx, int ny
  * the array: order them, e.g. by issuing them on one stream.
  *
  * Arguments, results and the other errors are those of cp_cutoff, without
- * workspace and workspace_bytes.                                            */
+ * workspace and workspace_bytes; CP_ERR_CUDA also when the array's device
+ * address cannot be looked up, for instance because the first call on a
+ * device was made while its stream was being captured.                     */
 CP_API int cp_cutoff_no_alloc(const float *atoms, int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h,
                               float cutoff, float bin_size, int capacity, float *V, void *stream);
 
@@ -470,9 +472,8 @@ CP_API int cp_eval_rsqrt(int kind, const float *x, float *y, int n, void *stream
 
 /* Microbenchmark of one SM pipe: every SM runs `warps` warps, each thread
  * issuing `iters` x 8 independent dependent-chain operations of kind
- * `kind` (0 = MUFU rsqrt.approx.ftz.f32, 1 = FP32 FFMA, 2 = MUFU ex2.approx,
- * 3 = FP32 FFMA in f32x2 pairs, 4 = half the chains as f32x2 pairs and half
- * as scalar FFMA, interleaved).  Writes the measured throughput in
+ * `kind` (0 = MUFU rsqrt.approx.ftz.f32, 1 = FP32 FFMA): the two rates
+ * behind the roofline of the direct and cutoff maps.  Writes the measured throughput in
  * operations per SM clock cycle (per-SM clock64 cycles, averaged over the
  * SMs) to *ops_per_clk and the kernel time to *ms.  Synchronous.
  * Returns CP_OK, CP_ERR_INVALID_ARGUMENT or CP_ERR_CUDA. */

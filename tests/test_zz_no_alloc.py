@@ -3,11 +3,13 @@ memory (their device memory belongs to another allocator, or they may not
 allocate once running).  Its scratch is a fixed 16 MiB array inside the
 library, shared by every call on a device.
 
-Checked through the C ABI against the existing entry point cp_cutoff, on two
-calls in a row with different inputs (the second call finds the first
-call's bins in the shared array), within the accuracy bound the other
-parity tests use: |dV| <= 2e-4 * sum_{r<c} |q|/r.  This file is collected
-last so that a failure here cannot hide failures elsewhere."""
+Checked through the C ABI against the existing entry point cp_cutoff on
+calls in a row with different inputs: a small map, then a large one, then
+the small one again, so that the last call runs over an array still holding
+the bins of a bigger map (anything left over from it would show), within the
+accuracy bound the other parity tests use: |dV| <= 2e-4 * sum_{r<c} |q|/r,
+and bit for bit.  This file is collected last so that a failure here cannot
+hide failures elsewhere."""
 import ctypes
 
 import numpy as np
@@ -38,10 +40,10 @@ def _cases():
     small = workloads.random_case(611, 1500, (24, 20, 17), h=0.5, origin=(-1.0, 0.5, 2.0), margin=4.0,
                                   cutoff=3.0, bin_size=1.0)
     big = workloads.make("cutoff_uniform")  # about 12 MiB of scratch: fits the 16 MiB array
-    return [small, big]
+    return [small, big, small]
 
 
-def test_no_alloc_matches_cutoff_on_two_calls_in_a_row():
+def test_no_alloc_matches_cutoff_on_calls_in_a_row():
     cases = _cases()
     devs = [torch.from_numpy(w.atoms).cuda() for w in cases]
     # two calls in a row on the shared array, then the existing entry point
