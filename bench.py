@@ -1,12 +1,21 @@
 #!/usr/bin/env python
 """Benchmark of the potential-map hot path on GB300.
 
-One step = the whole hot path over one batch of synthetic input:
-  * direct map: 128x128x64 grid (1,048,576 points) at h = 0.5 A, 40,000
-    off-lattice atoms with charges in [-1, 1]  ->  pair evaluations/s;
-  * cutoff map: 200^3 grid (8,000,000 points) at h = 0.5 A, 100,000 atoms
-    uniform in [0,100)^3 A, c = 12 A, 4 A bins, 16-slot bins: on-device
-    binning then the brick map  ->  grid points/s (and useful pairs/s).
+One step = the whole hot path over one batch of synthetic input, on the two
+largest single-GPU workloads:
+  * direct map (D1-D5): 200^3 grid (8,000,000 points) at h = 0.5 A, 100,000
+    off-lattice atoms from 200 Gaussian clusters, charges in
+    {-1, -0.5, 0.5, 1}  ->  pair evaluations/s (the headline ``value``);
+  * cutoff map (C1-C6): 400^3 grid (64,000,000 points) at h = 0.5 A,
+    800,000 atoms (70 % uniform, 30 % in 500 Gaussian clusters), c = 12 A,
+    4 A bins, capacity 0 (each bin a contiguous bin-sorted run, no fixed
+    slots): on-device binning then the brick map  ->  grid points/s and
+    useful pairs/s.
+After the timed steps every other workload is timed on its own with the
+pwwt.cn article's protocol (3 warm-ups, 10 timed runs): the 100x100 plane
+and the 128x128x64 direct maps, the 200^3 / 100k-atom cutoff map at
+capacity 0, and both cutoff maps with the lecture's fixed-capacity bins
+plus overflow list (capacity 8 and 16), each with its roofline fraction.
 Inputs are resident in HBM; L2 is flushed (a 256 MiB write) before every
 timed launch; each launch is timed with CUDA events on its stream.
 
@@ -36,10 +45,15 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 
 METRIC = "pair evals/s (direct Coulomb) and grid points/s at 12 Å cutoff, % of roofline"
-DIRECT_WL = "direct_3d"
-CUTOFF_WL = "cutoff_uniform"
+DIRECT_WL = "direct_protein"   # 200^3, 100k clustered atoms
+CUTOFF_WL = "cutoff_large"     # 400^3, 800k atoms, c = 12 A
 CAPACITY_DEFAULT = 0
 FLUSH_BYTES = 256 << 20
+# the other workloads, timed one by one after the steps
+SECONDARY_DIRECT = ["direct_plane", "direct_3d"]
+SECONDARY_CUTOFF = [("cutoff_uniform", 0), ("cutoff_uniform", 8), ("cutoff_uniform", 16),
+                    ("cutoff_large", 8), ("cutoff_large", 16)]
+CONFIG_NUMBER = {"direct_plane": 1, "direct_3d": 2, "direct_protein": 3, "cutoff_uniform": 4, "cutoff_large": 5}
 
 
 def env_rank():
@@ -51,9 +65,12 @@ def env_rank():
 
 def config_dict(wd, wc, capacity):
     return {
-        "workload": f"direct {wd.shape[0]}x{wd.shape[1]}x{wd.shape[2]} grid, {wd.n_atoms} atoms, h={wd.h} A; "
+        "workload": f"direct {wd.shape[0]}x{wd.shape[1]}x{wd.shape[2]} grid, {wd.n_atoms} clustered atoms, "
+        f"h={wd.h} A (config {CONFIG_NUMBER.get(wd.meta.get('key', ''), '?')}); "
         f"cutoff {wc.shape[0]}x{wc.shape[1]}x{wc.shape[2]} grid, {wc.n_atoms} atoms, c={wc.cutoff} A, "
-        f"{wc.bin_size} A bins",
+        f"{wc.bin_size} A bins, bin capacity {capacity} "
+        f"({'contiguous bin-sorted runs, no fixed slots' if capacity == 0 else 'fixed slots + overflow list'}) "
+        f"(config {CONFIG_NUMBER.get(wc.meta.get('key', ''), '?')})",
         "direct": {"grid": list(wd.shape), "atoms": wd.n_atoms, "h": wd.h, "pairs": wd.n_pairs,
                    "description": wd.description},
         "cutoff": {"grid": list(wc.shape), "atoms": wc.n_atoms, "h": wc.h, "cutoff": wc.cutoff,
@@ -62,6 +79,14 @@ def config_dict(wd, wc, capacity):
         "l2": "flushed before every timed launch (256 MiB write)",
         "parallelism": "one independent copy per rank (weak scaling)",
     }
+
+
+def make_workload(name):
+    import workloads
+
+    w = workloads.make(name)
+    w.meta["key"] = name
+    return w
 
 
 # ---------------------------------------------------------------------------
@@ -237,8 +262,8 @@ def run_reference(args):
     import oracle  # noqa: F401  (built on first use)
     import workloads
 
-    wd = workloads.make(DIRECT_WL)
-    wc = workloads.make(CUTOFF_WL)
+    wd = make_workload(DIRECT_WL)
+    wc = make_workload(CUTOFF_WL)
     threads = host_threads()
     # size one step for about 1.5 s so that warm-up + steps end within minutes
     _, n_pts, _ = oracle_direct_rate(wd, 1.5, threads)
@@ -281,9 +306,10 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # our arm
 
-def traffic_from_profile(kernel: str, source: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
-    kernel's source is unchanged since it was captured (else None)."""
+def traffic_from_profile(kernel: str, source: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if the kernel's source is unchanged since it was captured (else
+    None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -294,25 +320,74 @@ def traffic_from_profile(kernel: str, source: str):
         return None
     if not rec or rec.get("source_sha1") != sha:
         return None
-    return rec.get("dram_bytes_per_launch")
+    return (rec.get("per_workload") or {}).get(workload)
 
 
-def e2e_times(cp, wd, wc, Vd, Vc, ws, host_atoms_d, host_out_d, host_atoms_c, host_out_c, n, capacity):
+def e2e_times(cp, wd, wc, Vd, Vc, ws, host_atoms_d, host_out_d, host_atoms_c, host_out_c, n, capacity,
+              do_direct=True, do_cutoff=True):
     """Seconds per call of the public API with host buffers: pinned atoms in,
     host V out, copies and synchronisation included (one untimed call first)."""
-    cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
-    t0 = time.perf_counter()
-    for _ in range(n):
+    t_d = t_c = float("nan")
+    if do_direct:
         cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
-    t_d = (time.perf_counter() - t0) / n
-    cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, capacity, workspace=ws, out=Vc,
-              host_out=host_out_c)
-    t0 = time.perf_counter()
-    for _ in range(n):
+        t0 = time.perf_counter()
+        for _ in range(n):
+            cp.direct(host_atoms_d, wd.shape, wd.origin, wd.h, out=Vd, host_out=host_out_d)
+        t_d = (time.perf_counter() - t0) / n
+    if do_cutoff:
         cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, capacity, workspace=ws, out=Vc,
                   host_out=host_out_c)
-    t_c = (time.perf_counter() - t0) / n
+        t0 = time.perf_counter()
+        for _ in range(n):
+            cp.cutoff(host_atoms_c, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, capacity, workspace=ws,
+                      out=Vc, host_out=host_out_c)
+        t_c = (time.perf_counter() - t0) / n
     return t_d, t_c
+
+
+class Roofline:
+    """Per-SM bounds behind every roofline fraction in the line, from the
+    pipe rates measured on this GPU in the same run and the SM clock sampled
+    during the timed steps."""
+
+    def __init__(self, r_mufu, r_ffma, n_sm, f_mhz, clock_basis):
+        self.r_mufu, self.r_ffma, self.n_sm, self.f_mhz, self.clock_basis = r_mufu, r_ffma, n_sm, f_mhz, clock_basis
+        self.sm_clk = n_sm * f_mhz * 1e6  # SM clock cycles per second, one GPU
+        # direct: per pair at least 1 SFU rsqrt, 3 FP32 ops (dx, r^2,
+        # accumulate) and 4 issue slots: pairs/clk/SM = min(R_sfu, R_fp32/3, 128/4)
+        self.direct_sfu = min(r_mufu, r_ffma / 3.0, 32.0)
+        # the same pair with its rsqrt split between the SFU and the FMA pipe
+        # (estimate + two Newton steps: 6 FP32 ops): the best share f solves
+        # (1 - f)/R_sfu = (3 + 6f)/R_fp32
+        self.f_split = (r_ffma - 3.0 * r_mufu) / (r_ffma + 6.0 * r_mufu)
+        self.direct_split = r_mufu / (1.0 - self.f_split)
+        # cutoff: a useful pair needs 1 SFU rsqrt and about 11 FP32 ops (dx,
+        # dy, dz, three for r^2, compare, two for g, subtract, accumulate):
+        # useful pairs/clk/SM = min(R_sfu, R_fp32/11)
+        self.useful = min(r_mufu, r_ffma / 11.0)
+        # tighter: dy, dz and the row sums amortised over a thread's points,
+        # 8 issue slots and one SFU op per useful pair: min(R_sfu, 128/8)
+        self.useful_tight = min(r_mufu, 16.0)
+
+    def direct(self, pairs_per_s, world=1):
+        peak = self.direct_split * self.sm_clk * world
+        peak_sfu = self.direct_sfu * self.sm_clk * world
+        return {"achieved": pairs_per_s, "peak": peak, "frac": pairs_per_s / peak,
+                "peak_sfu_only": peak_sfu, "frac_sfu_only": pairs_per_s / peak_sfu}
+
+    def cutoff(self, useful_per_s, world=1):
+        peak = self.useful * self.sm_clk * world
+        tight = self.useful_tight * self.sm_clk * world
+        return {"achieved": useful_per_s, "peak": peak, "unit": "useful pair evals/s",
+                "frac": useful_per_s / peak,
+                "time_vs_useful_pair_roofline": peak / useful_per_s if useful_per_s > 0 else None,
+                "time_vs_tight_bound": tight / useful_per_s if useful_per_s > 0 else None}
+
+
+def bin_bytes_of(L, n_atoms, capacity):
+    """HBM bytes binning must move at least: atoms in, bin-sorted atoms and
+    indices out, counts and starts, fixed-capacity slots out."""
+    return 16 * n_atoms * 2 + 4 * n_atoms + 8 * int(L.nbins) + 16 * capacity * int(L.nbins)
 
 
 def run_ours(args):
@@ -328,14 +403,13 @@ def run_ours(args):
         dist.init_process_group("nccl", rank=rank, world_size=world, device_id=device)
 
     import direct_coulomb_summation_gb300 as cp
-    import workloads
 
     lib = cp.library()
     props = torch.cuda.get_device_properties(device)
     n_sm = props.multi_processor_count
 
-    wd = workloads.make(DIRECT_WL)
-    wc = workloads.make(CUTOFF_WL)
+    wd = make_workload(args.direct_workload)
+    wc = make_workload(args.cutoff_workload)
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
 
@@ -367,15 +441,17 @@ def run_ours(args):
     # roofline denominators: per-SM pipe rates measured on this GPU
     r_mufu, _ = cp.probe_pipe_rate("mufu_rsqrt", 32, 4096)
     r_ffma, _ = cp.probe_pipe_rate("ffma", 32, 4096)
-    # cutoff work accounting (not timed)
-    counts = {"useful": 0, "evaluated": 0, "examined": 0}
-    if args.only in ("both", "cutoff"):
-        counts = cp.cutoff_pair_counts(ac, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity,
-                                       workspace=ws)
-
-    sampler = ClockSampler(gpu_id_for(torch, device))
     do_direct = args.only in ("both", "direct")
     do_cutoff = args.only in ("both", "cutoff")
+    # cutoff work accounting (not timed)
+    counts = {"useful": 0, "evaluated": 0, "examined": 0}
+    stats = None
+    if do_cutoff:
+        counts = cp.cutoff_pair_counts(ac, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity,
+                                       workspace=ws)
+        stats = cp.cutoff_stats(ws, wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity)
+
+    sampler = ClockSampler(gpu_id_for(torch, device))
     for _ in range(args.warmup):
         flush.fill_(1)
         if do_direct:
@@ -422,6 +498,35 @@ def run_ours(args):
         time.sleep(0.5)  # let the sampler start before the steps
         ev, t_wall, launches, clocks = timed_steps(sampler)
         clocks = dict(clocks, remeasured_after={"reasons": first.get("reasons"), "sm_mhz": first.get("sm_mhz")})
+
+    t_direct = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    t_bin = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+    t_map = sum(e[3].elapsed_time(e[4]) for e in ev) / 1e3
+    # medians of the per-step leg times (ms), beside the means that the rates use
+    med_direct = float(np.median([e[0].elapsed_time(e[1]) for e in ev]))
+    med_cut = float(np.median([e[2].elapsed_time(e[4]) for e in ev]))
+    med_map = float(np.median([e[3].elapsed_time(e[4]) for e in ev]))
+    med_bin = float(np.median([e[2].elapsed_time(e[3]) for e in ev]))
+    t_direct, t_bin, t_map, t_wall, med_direct, med_cut, med_map, med_bin = max_over_ranks(
+        [t_direct, t_bin, t_map, t_wall, med_direct, med_cut, med_map, med_bin], device)
+    t_direct, t_bin, t_map = (max(t, 1e-12) for t in (t_direct, t_bin, t_map))
+    K = args.steps
+    direct_rate = float(wd.n_pairs) * world * K / t_direct
+    t_cut = t_bin + t_map
+    points_rate = float(wc.n_points) * world * K / t_cut
+
+    f_mhz = clocks.get("sm_mhz") or 2070.0
+    clock_basis = "median SM clock sampled during the timed steps" if clocks.get("sm_mhz") else "max SM clock"
+    roof = Roofline(r_mufu, r_ffma, n_sm, f_mhz, clock_basis)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    hbm_basis = "of measured" if "hbm_gbs" in peaks else "of fallback"
+
     # the cutoff leg again as one captured CUDA graph (binning's six launches
     # and the map replayed without per-launch host overhead)
     t_graph_cut = None
@@ -444,109 +549,38 @@ def run_ours(args):
             torch.cuda.synchronize()
             tg.append(e0.elapsed_time(e1))
         t_graph_cut = float(np.mean(tg)) / 1e3
-    # multilevel long-range part on the cutoff workload (reported beside the
-    # step, not part of it): cp_msm_longrange adding V_long to the cutoff map
+        del graph
+
+    # every other workload, one at a time (3 warm-ups, 10 timed runs, L2
+    # flushed before each); not part of the step
+    secondary = None
+    if not args.no_secondary:
+        sec_sampler = ClockSampler(gpu_id_for(torch, device))
+        sec_sampler.mark_begin()
+        secondary = measure_secondary(cp, lib, torch, device, stream, flush, roof, hbm_peak, hbm_basis,
+                                      do_direct, do_cutoff, args.capacity, {args.cutoff_workload: wc})
+        sec_sampler.mark_end()
+        secondary["clocks"] = sec_sampler.stop()
+
+    # multilevel long-range part on the 200^3 / 100k-atom cutoff workload
+    # (reported beside the step, not part of it)
     msm = None
     if do_cutoff and not args.no_msm:
-        lo, hi = cp.atom_bounds(ac)
-        dom = (cp._vec3(lo), cp._vec3(hi))
-        h0 = float(np.float32(args.msm_lattice))
-        ML = cp.msm_layout(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, h0, (lo, hi))
-        mws = torch.empty(int(ML.total_bytes), dtype=torch.uint8, device=device)
-
-        def run_msm():
-            call(lib.cp_msm_longrange(ac.data_ptr(), wc.n_atoms, *gc, *dom, cut[0], h0, mws.data_ptr(),
-                                      int(ML.total_bytes), Vc.data_ptr(), 1, sh), "cp_msm_longrange")
-
-        for _ in range(3):
-            run_msm()
-        torch.cuda.synchronize()
-        n_msm = max(3, min(args.steps, 20))
-        tm = []
-        m_launch0 = lib.cp_launch_count()
-        for _ in range(n_msm):
-            flush.fill_(7)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            run_msm()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            tm.append(e0.elapsed_time(e1))
-        m_launches = (lib.cp_launch_count() - m_launch0) // n_msm
-        levels = int(ML.levels)
-        nodes = [int(ML.n[l][0]) * int(ML.n[l][1]) * int(ML.n[l][2]) for l in range(levels)]
-        # algorithmic FMAs of the lattice cutoffs: every node of every level
-        # below the top times the stencil's taps, plus the dense top level
-        fma = sum(nodes[:-1]) * int(ML.taps) + nodes[-1] ** 2
-        msm = {"lattice_h": h0, "levels": levels, "nodes": nodes, "stencil_taps": int(ML.taps),
-               "ms_longrange": float(np.median(tm)), "launches_per_call": int(m_launches),
-               "lattice_cutoff_fma_per_call": fma}
+        msm = measure_msm(cp, lib, torch, device, stream, flush, args, roof, call)
     status = cp.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status:#x} after the timed steps")
 
-    t_direct = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
-    t_bin = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
-    t_map = sum(e[3].elapsed_time(e[4]) for e in ev) / 1e3
-    # medians of the per-step leg times (ms), beside the means that the rates use
-    med_direct = float(np.median([e[0].elapsed_time(e[1]) for e in ev]))
-    med_cut = float(np.median([e[2].elapsed_time(e[4]) for e in ev]))
-    med_map = float(np.median([e[3].elapsed_time(e[4]) for e in ev]))
-    t_direct, t_bin, t_map, t_wall, med_direct, med_cut, med_map = max_over_ranks(
-        [t_direct, t_bin, t_map, t_wall, med_direct, med_cut, med_map], device)
-    t_direct, t_bin, t_map = (max(t, 1e-12) for t in (t_direct, t_bin, t_map))
-    K = args.steps
-    direct_pairs = float(wd.n_pairs) * world * K
-    direct_rate = direct_pairs / t_direct
-    t_cut = t_bin + t_map
-    points_rate = float(wc.n_points) * world * K / t_cut
-
-    # rooflines -------------------------------------------------------------
-    f_mhz = clocks.get("sm_mhz") or 2070.0
-    clock_basis = "median SM clock sampled during the timed steps" if clocks.get("sm_mhz") else "max SM clock"
-    sm_clk = n_sm * f_mhz * 1e6 * world  # SM clock cycles per second, whole job
-    # direct: per pair at least 1 SFU rsqrt, 3 FP32 ops (dx, r^2, accumulate)
-    # and 4 issue slots: pairs/clk/SM = min(R_sfu, R_fp32/3, 128/4)
-    per_sm_direct = min(r_mufu, r_ffma / 3.0, 32.0)
-    peak_direct = per_sm_direct * sm_clk
-    achieved_direct = direct_rate
-    # the same pair with its rsqrt split between the SFU and the FMA pipe
-    # (estimate + two Newton steps: 6 FP32 ops): best split f solves
-    # (1 - f)/R_sfu = (3 + 6f)/R_fp32
-    f_split = (r_ffma - 3.0 * r_mufu) / (r_ffma + 6.0 * r_mufu)
-    per_sm_split = r_mufu / (1.0 - f_split)
-    # cutoff: a useful pair needs 1 SFU rsqrt and about 11 FP32 ops (dx, dy,
-    # dz, three for r^2, compare, two for g, subtract, accumulate):
-    # useful pairs/clk/SM = min(R_sfu, R_fp32/11)
-    per_sm_useful = min(r_mufu, r_ffma / 11.0)
-    useful_rate = counts["useful"] * world * K / t_map
-    peak_useful = per_sm_useful * sm_clk
-    # tighter: with dy, dz and the row sums amortised over a thread's points,
-    # 8 issue slots and one SFU op per useful pair: min(R_sfu, 128/8)
-    per_sm_useful_tight = min(r_mufu, 16.0)
-    # binning: HBM bytes it must move at least (atoms in, bin-sorted atoms and
-    # indices out, counts and starts, fixed-capacity slots out)
-    L = cp.cutoff_layout(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity)
-    bin_bytes = 16 * wc.n_atoms * 2 + 4 * wc.n_atoms + 8 * int(L.nbins) + 16 * args.capacity * int(L.nbins)
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except (OSError, ValueError):
-        pass
-    hbm_peak = peaks.get("hbm_gbs", 6800.0)
-    hbm_basis = "of measured" if "hbm_gbs" in peaks else "of fallback"
-
     # end to end through the public API with host buffers ---------------------
-    host_atoms_d = torch.from_numpy(wd.atoms).pin_memory()
-    host_out_d = torch.empty(Vd.shape, dtype=torch.float32, pin_memory=True)
-    host_atoms_c = torch.from_numpy(wc.atoms).pin_memory()
-    host_out_c = torch.empty(Vc.shape, dtype=torch.float32, pin_memory=True)
-    n_e2e = max(3, min(K, 10))
+    n_e2e = max(3, min(K, 5))
     t_e2e_d = t_e2e_c = float("nan")
     if not args.no_e2e:
+        host_atoms_d = torch.from_numpy(wd.atoms).pin_memory()
+        host_out_d = torch.empty(Vd.shape, dtype=torch.float32, pin_memory=True)
+        host_atoms_c = torch.from_numpy(wc.atoms).pin_memory()
+        host_out_c = torch.empty(Vc.shape, dtype=torch.float32, pin_memory=True)
         t_e2e_d, t_e2e_c = e2e_times(cp, wd, wc, Vd, Vc, ws, host_atoms_d, host_out_d, host_atoms_c, host_out_c,
-                                     n_e2e, args.capacity)
+                                     n_e2e, args.capacity, do_direct, do_cutoff)
         t_e2e_d, t_e2e_c = max_over_ranks([t_e2e_d, t_e2e_c], device)
 
     if rank != 0:
@@ -567,9 +601,17 @@ def run_ours(args):
                "single_core": {"value": srate, "unit": "pair evals/s", "cores": 1,
                                "sample": f"the same sum at {s_pts} points on one thread ({sdt:.1f} s)"},
                "cutoff": {"value": crate, "unit": "grid points/s",
-                          "sample": f"fp64 binned cutoff sum at {c_pts} seeded points ({cdt:.1f} s)"}}
+                          "sample": f"fp64 binned cutoff sum at {c_pts} seeded points of the {tuple(wc.shape)} "
+                                    f"grid ({cdt:.1f} s)"}}
 
-    traffic = traffic_from_profile("direct_kernel", "direct_coulomb_summation_gb300/csrc/cp_direct.cu")
+    traffic = traffic_from_profile("direct_kernel", "direct_coulomb_summation_gb300/csrc/cp_direct.cu",
+                                   args.direct_workload)
+    traffic_map = traffic_from_profile("cutoff_brick_kernel", "direct_coulomb_summation_gb300/csrc/cp_cutoff.cu",
+                                       args.cutoff_workload)
+    rd = roof.direct(direct_rate, world)
+    useful_rate = counts["useful"] * world * K / t_map
+    L = cp.cutoff_layout(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity)
+    bin_bytes = bin_bytes_of(L, wc.n_atoms, args.capacity)
     line = {
         "metric": METRIC,
         "value": direct_rate,
@@ -587,66 +629,68 @@ def run_ours(args):
         "roofline": {
             "bound": "alu",
             "kernel": "direct_kernel (cp_direct)",
-            "achieved": achieved_direct,
-            "peak": per_sm_split * sm_clk,
+            "workload": wd.description,
+            "achieved": rd["achieved"],
+            "peak": rd["peak"],
             "unit": "pair evals/s",
-            "frac": achieved_direct / (per_sm_split * sm_clk),
+            "frac": rd["frac"],
             "traffic": traffic,
-            "peak_basis": f"{n_sm} SMs x {per_sm_split:.1f} pairs/clk/SM x {f_mhz:.0f} MHz ({clock_basis}): "
-                          f"the pair (1 rsqrt, 3 FP32 ops) with its rsqrt shared between the SFU ({r_mufu:.2f}/clk/SM "
-                          f"measured) and the FMA pipe (magic-constant estimate + two Newton steps, 6 FP32 ops; "
-                          f"FFMA {r_ffma:.1f} lanes/clk/SM measured) at the best share {f_split:.2f}, "
-                          f"(1 - f)/R_sfu = (3 + 6f)/R_fp32",
-            "peak_sfu_only": peak_direct,
-            "frac_sfu_only": achieved_direct / peak_direct,
-            "sfu_only_basis": f"{n_sm} SMs x {per_sm_direct:.2f} pairs/clk/SM = min(SFU rsqrt {r_mufu:.2f}, "
+            "peak_basis": f"{n_sm} SMs x {roof.direct_split:.1f} pairs/clk/SM x {f_mhz:.0f} MHz ({clock_basis}): "
+                          f"the pair (1 rsqrt, 3 FP32 ops) with its rsqrt shared between the SFU "
+                          f"({r_mufu:.2f}/clk/SM measured) and the FMA pipe (magic-constant estimate + two Newton "
+                          f"steps, 6 FP32 ops; FFMA {r_ffma:.1f} lanes/clk/SM measured) at the best share "
+                          f"{roof.f_split:.2f}, (1 - f)/R_sfu = (3 + 6f)/R_fp32",
+            "peak_sfu_only": rd["peak_sfu_only"],
+            "frac_sfu_only": rd["frac_sfu_only"],
+            "sfu_only_basis": f"{n_sm} SMs x {roof.direct_sfu:.2f} pairs/clk/SM = min(SFU rsqrt {r_mufu:.2f}, "
                               f"FFMA {r_ffma:.1f}/3, issue 128/4): the scope table's bound for rsqrt on the SFU "
                               f"alone, which the kernel exceeds by moving a share of the rsqrts to the FMA pipe",
         },
         "direct": {
+            "config": CONFIG_NUMBER.get(args.direct_workload),
             "pair_evals_per_s": direct_rate,
             "grid_points_per_s": float(wd.n_points) * world * K / t_direct,
             "ms": 1e3 * t_direct / K,
             "ms_median": med_direct if do_direct else None,
+            "plan": list(cp.direct_plan(wd.n_atoms, wd.shape)),
         },
         "cutoff": {
+            "config": CONFIG_NUMBER.get(args.cutoff_workload),
+            "capacity": args.capacity,
             "grid_points_per_s": points_rate,
             "useful_pairs_per_s": counts["useful"] * world * K / t_cut,
             "evaluated_pairs_per_s": counts["evaluated"] * world * K / t_cut,
             "examined_pairs_per_s": counts["examined"] * world * K / t_cut,
             "pairs_per_step": counts,
+            "evaluated_per_useful": counts["evaluated"] / counts["useful"] if counts["useful"] else None,
+            "binning_stats": stats,
+            "overflow_atoms": None if (stats is None or args.capacity == 0) else stats["n_overflow"],
+            "binning_note": "capacity 0 has no fixed slots: every atom is read from its bin's contiguous run, so "
+                            "n_overflow counts all binned atoms" if args.capacity == 0 else
+                            "n_overflow = atoms past the fixed slots, read by the overflow sweep",
             "ms": 1e3 * t_cut / K,
             "ms_median": med_cut if do_cutoff else None,
             "ms_binning": 1e3 * t_bin / K,
+            "ms_binning_median": med_bin if do_cutoff else None,
             "ms_map": 1e3 * t_map / K,
             "ms_map_median": med_map if do_cutoff else None,
             "ms_as_cuda_graph": None if t_graph_cut is None else 1e3 * t_graph_cut,
-            "roofline_map": {
-                "bound": "alu", "kernel": "cutoff_brick_kernel (cp_cutoff_map)",
-                "achieved": useful_rate, "peak": peak_useful, "unit": "useful pair evals/s",
-                "frac": useful_rate / peak_useful,
-                "time_vs_useful_pair_roofline": peak_useful / useful_rate if useful_rate > 0 else None,
-                "peak_basis": f"{n_sm} SMs x {per_sm_useful:.2f} useful pairs/clk/SM = min(SFU {r_mufu:.2f}, "
-                              f"FFMA {r_ffma:.1f}/11) x {f_mhz:.0f} MHz",
-                "time_vs_tight_bound": per_sm_useful_tight * sm_clk / useful_rate if useful_rate > 0 else None,
-                "tight_basis": f"min(SFU {r_mufu:.2f}, 128 issue/8) = {per_sm_useful_tight:.1f} useful pairs/clk/SM",
-            },
+            "roofline_map": dict(
+                roof.cutoff(useful_rate, world), bound="alu", kernel="cutoff_brick_kernel (cp_cutoff_map)",
+                traffic=traffic_map,
+                peak_basis=f"{n_sm} SMs x {roof.useful:.2f} useful pairs/clk/SM = min(SFU {r_mufu:.2f}, "
+                           f"FFMA {r_ffma:.1f}/11) x {f_mhz:.0f} MHz",
+                tight_basis=f"min(SFU {r_mufu:.2f}, 128 issue/8) = {roof.useful_tight:.1f} useful pairs/clk/SM"),
             "roofline_binning": {
                 "bound": "hbm", "achieved": bin_bytes * world * K / t_bin / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                "frac": bin_bytes * world * K / t_bin / 1e9 / hbm_peak, "traffic": None,
+                "frac": bin_bytes * world * K / t_bin / 1e9 / hbm_peak,
+                "traffic": traffic_from_profile("binning", "direct_coulomb_summation_gb300/csrc/cp_cutoff.cu",
+                                                args.cutoff_workload),
                 "algorithmic_bytes": bin_bytes, "peak_basis": f"hbm_gbs {hbm_basis}",
             },
         },
-        "msm": None if msm is None else dict(
-            msm,
-            ms_map=1e3 * t_cut / K + msm["ms_longrange"],
-            grid_points_per_s_map=float(wc.n_points) * world / (t_cut / K + 1e-3 * msm["ms_longrange"]),
-            fp32_fma_per_s_longrange=msm["lattice_cutoff_fma_per_call"] / (1e-3 * msm["ms_longrange"]),
-            frac_of_fp32_fma=msm["lattice_cutoff_fma_per_call"] / (1e-3 * msm["ms_longrange"]) / (r_ffma * sm_clk / world),
-            basis="the whole cp_msm_longrange call (cell sort, anterpolation, restriction, lattice cutoffs, "
-                  "prolongation, interpolation) against the FP32 FMA rate for its lattice-cutoff FMAs alone; "
-                  "ms_map adds the cutoff leg (binning + short-range map): the multilevel approximation of the "
-                  "full direct sum on this grid"),
+        "secondary": secondary,
+        "msm": msm,
         "cpu_baseline": cpu,
         "e2e": {
             "value": float(wd.n_pairs) * world / t_e2e_d,
@@ -674,6 +718,145 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def _timed_runs(torch, stream, flush, fns, reps=10, warm=3):
+    """The pwwt.cn article's protocol: warm-ups, then `reps` runs with L2
+    flushed before each; `fns` run back to back and each is timed with CUDA
+    events on `stream`.  Returns per-fn lists of ms."""
+    for _ in range(warm):
+        for fn in fns:
+            fn()
+    out = [[] for _ in fns]
+    for r in range(reps):
+        flush.fill_(r & 0x7F)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+        ev[0].record(stream)
+        for i, fn in enumerate(fns):
+            fn()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        for i in range(len(fns)):
+            out[i].append(ev[i].elapsed_time(ev[i + 1]))
+    return out
+
+
+def measure_secondary(cp, lib, torch, device, stream, flush, roof, hbm_peak, hbm_basis, do_direct, do_cutoff,
+                      head_capacity, workloads_done=None):
+    sh = stream.cuda_stream
+    res = {"protocol": "3 warm-ups, 10 timed runs each, 256 MiB L2 flush before each run, CUDA events; "
+                       "not part of the timed steps", "direct": {}, "cutoff": {}}
+
+    def call(rc, where):
+        if rc != 0:
+            raise cp.CpError(rc, where)
+
+    if do_direct:
+        for name in SECONDARY_DIRECT:
+            w = make_workload(name)
+            a = torch.from_numpy(w.atoms).to(device)
+            V = torch.empty((w.shape[2], w.shape[1], w.shape[0]), dtype=torch.float32, device=device)
+            g = cp._grid(w.shape, w.origin, w.h)
+            (ts,) = _timed_runs(torch, stream, flush, [
+                lambda: call(lib.cp_direct(a.data_ptr(), w.n_atoms, *g, V.data_ptr(), sh), "cp_direct")])
+            mean = float(np.mean(ts))
+            rate = w.n_pairs / (mean * 1e-3)
+            rd = roof.direct(rate)
+            res["direct"][name] = {
+                "config": CONFIG_NUMBER[name], "workload": w.description, "grid": list(w.shape), "atoms": w.n_atoms,
+                "pairs": w.n_pairs, "ms": mean, "ms_median": float(np.median(ts)), "pair_evals_per_s": rate,
+                "grid_points_per_s": w.n_points / (mean * 1e-3), "roofline_frac": rd["frac"],
+                "frac_sfu_only": rd["frac_sfu_only"], "plan": list(cp.direct_plan(w.n_atoms, w.shape))}
+            del a, V
+    if do_cutoff:
+        cache = dict(workloads_done or {})
+        for name, K in SECONDARY_CUTOFF:
+            if name == CUTOFF_WL and K == head_capacity:
+                continue
+            if name not in cache:
+                cache[name] = make_workload(name)
+            w = cache[name]
+            a = torch.from_numpy(w.atoms).to(device)
+            V = torch.empty((w.shape[2], w.shape[1], w.shape[0]), dtype=torch.float32, device=device)
+            nbytes = cp.cutoff_workspace_bytes(w.n_atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, K)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+            g = cp._grid(w.shape, w.origin, w.h)
+            cut = [float(np.float32(w.cutoff)), float(np.float32(w.bin_size)), K]
+            counts = cp.cutoff_pair_counts(a, w.shape, w.origin, w.h, w.cutoff, w.bin_size, K, workspace=ws)
+            stats = cp.cutoff_stats(ws, w.n_atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, K)
+            tb, tm = _timed_runs(torch, stream, flush, [
+                lambda: call(lib.cp_bin_atoms(a.data_ptr(), w.n_atoms, *g, *cut, ws.data_ptr(), nbytes, sh),
+                             "cp_bin_atoms"),
+                lambda: call(lib.cp_cutoff_map(a.data_ptr(), w.n_atoms, *g, *cut, ws.data_ptr(), nbytes,
+                                               V.data_ptr(), sh), "cp_cutoff_map")])
+            mb, mm = float(np.mean(tb)), float(np.mean(tm))
+            L = cp.cutoff_layout(w.n_atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, K)
+            bb = bin_bytes_of(L, w.n_atoms, K)
+            entry = {
+                "config": CONFIG_NUMBER[name], "workload": w.description, "capacity": K,
+                "layout": "contiguous bin-sorted runs" if K == 0 else f"{K} fixed slots per bin + overflow list",
+                "ms": mb + mm, "ms_median": float(np.median(np.asarray(tb) + np.asarray(tm))),
+                "ms_binning": mb, "ms_map": mm, "ms_map_median": float(np.median(tm)),
+                "grid_points_per_s": w.n_points / ((mb + mm) * 1e-3),
+                "useful_pairs_per_s": counts["useful"] / ((mb + mm) * 1e-3),
+                "pairs": counts, "evaluated_per_useful": counts["evaluated"] / max(counts["useful"], 1),
+                "binning_stats": stats,
+                "overflow_atoms": None if K == 0 else stats["n_overflow"],
+                "roofline_map": roof.cutoff(counts["useful"] / (mm * 1e-3)),
+                "roofline_binning": {"bound": "hbm", "achieved": bb / (mb * 1e-3) / 1e9, "peak": hbm_peak,
+                                     "unit": "GB/s", "frac": bb / (mb * 1e-3) / 1e9 / hbm_peak,
+                                     "algorithmic_bytes": bb, "peak_basis": f"hbm_gbs {hbm_basis}"},
+            }
+            res["cutoff"][f"{name}/capacity_{K}"] = entry
+            del a, V, ws
+    torch.cuda.synchronize()
+    return res
+
+
+def measure_msm(cp, lib, torch, device, stream, flush, args, roof, call):
+    """cp_msm_longrange adding V_long to the 200^3 / 100k-atom cutoff map."""
+    sh = stream.cuda_stream
+    w = make_workload("cutoff_uniform")
+    a = torch.from_numpy(w.atoms).to(device)
+    V = torch.empty((w.shape[2], w.shape[1], w.shape[0]), dtype=torch.float32, device=device)
+    g = cp._grid(w.shape, w.origin, w.h)
+    cut = [float(np.float32(w.cutoff)), float(np.float32(w.bin_size)), 0]
+    nbytes = cp.cutoff_workspace_bytes(w.n_atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    lo, hi = cp.atom_bounds(a)
+    dom = (cp._vec3(lo), cp._vec3(hi))
+    h0 = float(np.float32(args.msm_lattice))
+    ML = cp.msm_layout(w.n_atoms, w.shape, w.origin, w.h, w.cutoff, h0, (lo, hi))
+    mws = torch.empty(int(ML.total_bytes), dtype=torch.uint8, device=device)
+
+    def run_cut():
+        call(lib.cp_cutoff(a.data_ptr(), w.n_atoms, *g, *cut, ws.data_ptr(), nbytes, V.data_ptr(), sh), "cp_cutoff")
+
+    def run_msm():
+        call(lib.cp_msm_longrange(a.data_ptr(), w.n_atoms, *g, *dom, cut[0], h0, mws.data_ptr(),
+                                  int(ML.total_bytes), V.data_ptr(), 1, sh), "cp_msm_longrange")
+
+    m_launch0 = lib.cp_launch_count()
+    tc, tm = _timed_runs(torch, stream, flush, [run_cut, run_msm], reps=max(3, min(args.steps, 20)))
+    n_calls = 3 + max(3, min(args.steps, 20))
+    levels = int(ML.levels)
+    nodes = [int(ML.n[l][0]) * int(ML.n[l][1]) * int(ML.n[l][2]) for l in range(levels)]
+    # algorithmic FMAs of the lattice cutoffs: every node of every level
+    # below the top times the stencil's taps, plus the dense top level
+    fma = sum(nodes[:-1]) * int(ML.taps) + nodes[-1] ** 2
+    ms_l, ms_c = float(np.median(tm)), float(np.median(tc))
+    launches_cut = 7
+    return {"workload": w.description, "lattice_h": h0, "levels": levels, "nodes": nodes,
+            "stencil_taps": int(ML.taps), "ms_longrange": ms_l,
+            "launches_per_call": int((lib.cp_launch_count() - m_launch0) // n_calls - launches_cut),
+            "lattice_cutoff_fma_per_call": fma, "ms_map": ms_c + ms_l,
+            "grid_points_per_s_map": w.n_points / (1e-3 * (ms_c + ms_l)),
+            "fp32_fma_per_s_longrange": fma / (1e-3 * ms_l),
+            "frac_of_fp32_fma": fma / (1e-3 * ms_l) / (roof.r_ffma * roof.sm_clk),
+            "basis": "the whole cp_msm_longrange call (cell sort, anterpolation, restriction, lattice cutoffs, "
+                     "prolongation, interpolation) against the FP32 FMA rate for its lattice-cutoff FMAs alone; "
+                     "ms_map adds the cutoff map of the same grid (binning + short-range map, capacity 0): the "
+                     "multilevel approximation of the full direct sum on this grid"}
 
 
 def run_compare(args):
@@ -736,7 +919,7 @@ def run_compare(args):
         v["pair_evals_per_s"] = w.n_pairs / (v["ms"] * 1e-3)
         v["speedup_vs_sequential"] = seq_ms / v["ms"]
 
-    wc = workloads.make(CUTOFF_WL)
+    wc = workloads.make("cutoff_uniform")
     ac = torch.from_numpy(wc.atoms).to(device)
     Vc = torch.empty((wc.shape[2], wc.shape[1], wc.shape[0]), dtype=torch.float32, device=device)
     ws = torch.empty(max(cp.cutoff_workspace_bytes(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, 0),
@@ -761,7 +944,7 @@ def run_compare(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -771,6 +954,12 @@ def main(argv=None):
     ap.add_argument("--only", choices=["both", "direct", "cutoff"], default="both",
                     help="time one leg only (for profiling; the JSON line then covers that leg)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the per-workload timings after the steps (for profiling)")
+    ap.add_argument("--direct-workload", choices=["direct_plane", "direct_3d", "direct_protein"], default=DIRECT_WL,
+                    help="direct workload of the step (the default is the headline; others for profiling)")
+    ap.add_argument("--cutoff-workload", choices=["cutoff_uniform", "cutoff_large"], default=CUTOFF_WL,
+                    help="cutoff workload of the step (the default is the headline; others for profiling)")
     ap.add_argument("--compare", action="store_true",
                     help="time the pages' own strategies against this library (one JSON line) and exit")
     ap.add_argument("--capacity", type=int, choices=[0, 8, 16], default=CAPACITY_DEFAULT,

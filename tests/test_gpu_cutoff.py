@@ -102,26 +102,67 @@ def test_cutoff_host_buffers_match_device():
     assert not vh.is_cuda and torch.equal(vh, vd.cpu())
 
 
-def test_cutoff_uniform_workload_sampled():
-    """100 000 atoms, 200^3 grid, c = 12 A, 4 A bins: full map on the GPU,
+def _benchmark_call(w, K):
+    """The cutoff map as bench.py times it: cp_bin_atoms then cp_cutoff_map
+    through the C ABI on one caller-owned workspace, c and b from the
+    workload (12 A, 4 A)."""
+    lib = cp.library()
+    a = to_dev(w.atoms)
+    V = torch.full((w.shape[2], w.shape[1], w.shape[0]), float("nan"), device="cuda")
+    nbytes = cp.cutoff_workspace_bytes(w.n_atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, K)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    g = cp._grid(w.shape, w.origin, w.h)
+    cut = (float(np.float32(w.cutoff)), float(np.float32(w.bin_size)), K)
+    s = torch.cuda.current_stream().cuda_stream
+    assert lib.cp_bin_atoms(a.data_ptr(), w.n_atoms, *g, *cut, ws.data_ptr(), nbytes, s) == 0
+    assert lib.cp_cutoff_map(a.data_ptr(), w.n_atoms, *g, *cut, ws.data_ptr(), nbytes, V.data_ptr(), s) == 0
+    torch.cuda.synchronize()
+    assert cp.device_status() == 0
+    return V
+
+
+@pytest.mark.parametrize("K", [0, 16])
+def test_cutoff_uniform_workload_sampled(K):
+    """100 000 atoms, 200^3 grid, c = 12 A, 4 A bins (capacity 0 is the
+    benchmarked layout): full map on the GPU in the benchmark's two calls,
     4096 seeded points by the brute-force oracle."""
     w = workloads.make("cutoff_uniform")
-    V = _run(w, w.cutoff, w.bin_size)
+    V = _benchmark_call(w, K)
     pts = workloads.sample_points(w.shape, 4096, seed=4097)
     ref, bound = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, w.cutoff, points=pts)
     got = V.reshape(-1)[torch.from_numpy(flat_index(w.shape, pts)).cuda()].cpu().numpy()
     assert_within_bound(got, ref, bound, w.name)
+    assert torch.isfinite(V).all()
 
 
-def test_cutoff_large_workload_sampled():
-    """800 000 atoms (30 % in Gaussian clusters), 400^3 grid: 4096 seeded points
-    by the binned oracle (bit-identical to brute force by its pins)."""
+@pytest.mark.parametrize("K", [0, 16])
+def test_cutoff_uniform_workload_brick_layers(K):
+    """Whole brick layers of the 200^3 map (the first, a middle and the last
+    8 planes: every brick of them, edges included) against the binned oracle
+    at every point."""
+    w = workloads.make("cutoff_uniform")
+    V = _benchmark_call(w, K)
+    nx, ny, nz = w.shape
+    for z0 in (0, 96, nz - 8):
+        ij = np.stack(np.meshgrid(np.arange(nx), np.arange(ny), indexing="xy"), -1).reshape(-1, 2)
+        pts = np.concatenate([np.column_stack([ij, np.full(len(ij), z)]) for z in range(z0, z0 + 8)])
+        ref, bound = oracle.cutoff_binned(w.atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, points=pts)
+        got = V.reshape(-1)[torch.from_numpy(flat_index(w.shape, pts)).cuda()].cpu().numpy()
+        assert_within_bound(got, ref, bound, f"{w.name} planes {z0}..{z0 + 7}")
+
+
+@pytest.mark.parametrize("K", [0, 16])
+def test_cutoff_large_workload_sampled(K):
+    """800 000 atoms (30 % in Gaussian clusters), 400^3 grid, c = 12 A, 4 A
+    bins, in the benchmark's two calls: 4096 seeded points by the binned
+    oracle (bit-identical to brute force by its pins)."""
     w = workloads.make("cutoff_large")
-    V = _run(w, w.cutoff, w.bin_size)
+    V = _benchmark_call(w, K)
     pts = workloads.sample_points(w.shape, 4096, seed=4098)
     ref, bound = oracle.cutoff_binned(w.atoms, w.shape, w.origin, w.h, w.cutoff, w.bin_size, points=pts)
     got = V.reshape(-1)[torch.from_numpy(flat_index(w.shape, pts)).cuda()].cpu().numpy()
     assert_within_bound(got, ref, bound, w.name)
+    assert torch.isfinite(V).all()
 
 
 def _pairs_within(w, c, rel):
