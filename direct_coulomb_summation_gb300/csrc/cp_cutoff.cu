@@ -24,13 +24,16 @@
 //     more than the capacity.
 //   * Consumer warp w owns sub-box w of the brick (8 x 4 x 4 points; each
 //     lane 4 consecutive x points as two f32x2 pairs).  For every stage each
-//     consumer warp tests all the stage's atoms against its own sub-box
-//     (distance to the box < c), copies those that pass into its own list
-//     (stage order), releases the stage and runs the list through the pair
-//     loop, adding the switched term
-//     q * (rsqrt(r^2) - (GC0 + r^2 (GC1 + r^2 GC2))) for r^2 < c^2.  The
-//     consumer warps never wait for one another: each may run ahead of the
-//     others by up to the ring's depth.
+//     consumer warp tests all the stage's atoms against its own sub-box,
+//     copies those that can reach it into its own list (stage order),
+//     releases the stage and runs the list through the pair loop.  An atom
+//     within c of every point of the sub-box ("full") adds q * rsqrt(r^2)
+//     per pair; its -q g(r) is a quartic polynomial in the point's position,
+//     added once per point at the end from 15 charge moments of the full
+//     atoms about the sub-box centre.  Any other listed atom adds the
+//     switched term q * (rsqrt(r^2) - (GC0 + r^2 (GC1 + r^2 GC2))) for
+//     r^2 < c^2.  The consumer warps never wait for one another: each may
+//     run ahead of the others by up to the ring's depth.
 //   * Unused fixed slots sit at 1e18 A and never pass the sub-box test,
 //     which replaces the lecture's stop-at-the-first-empty-slot rule.
 #include <cuda_runtime.h>
@@ -522,9 +525,22 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
     const int wy0 = kBrick * by + (warp & 1) * 4, wz0 = kBrick * bz + (warp >> 1) * 4;
     const float loy = fmaf((float)wy0, p.h, p.oy), hiy = fmaf((float)(wy0 + 3), p.h, p.oy);
     const float loz = fmaf((float)wz0, p.h, p.oz), hiz = fmaf((float)(wz0 + 3), p.h, p.oz);
+    // Centre of the sub-box (its middle point, index 8bx + 3.5, wy0 + 1.5,
+    // wz0 + 1.5), the expansion point of the full atoms' moments; REL:
+    // relative to the grid origin, like the listed atoms.
+    const float cxi = (float)(kBrick * bx) + 3.5f, cyi = (float)wy0 + 1.5f, czi = (float)wz0 + 1.5f;
+    const float cx = REL ? cxi * p.h : fmaf(cxi, p.h, p.ox);
+    const float cy = REL ? cyi * p.h : fmaf(cyi, p.h, p.oy);
+    const float cz = REL ? czi * p.h : fmaf(czi, p.h, p.oz);
     const unsigned below = (1u << lane) - 1u;
     float4 *list = &wlist[warp][0];
 
+    // Moments about the centre of the atoms within c of the whole sub-box
+    // (w = atom - centre, m = |w|^2; this lane's share of them):
+    // sum q, sum q w, sum q m, sum q m^2, sum q m w, sum q w w^T.
+    float mq = 0.f, mqx = 0.f, mqy = 0.f, mqz = 0.f, mqm = 0.f, mqmm = 0.f;
+    float mrx = 0.f, mry = 0.f, mrz = 0.f;
+    float mtxx = 0.f, mtxy = 0.f, mtxz = 0.f, mtyy = 0.f, mtyz = 0.f, mtzz = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     unsigned long long n_real = 0, n_near = 0, n_useful = 0;  // COUNT only
     for (int seq = 0;; ++seq) {
@@ -532,9 +548,11 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
         const bool got = mbar_wait(&full[s], (uint32_t)((seq / kBrickStages) & 1), p.status);
         const int n = got ? stage_n[s] : -1;
         if (n < 0) break;  // end of the stream (or a wait that ran out: recorded)
-        // (1) every atom of the stage against this warp's sub-box; those that
-        // can reach it are copied, in stage order, to the warp's own list
-        int cnt = 0;
+        // (1) every atom of the stage against this warp's sub-box.  An atom
+        // within c of every point of it ("full") goes to the front of the
+        // warp's list, one that can reach only some of its points
+        // ("partial") to the back, both in stage order.
+        int cnt_f = 0, cnt_p = 0;
         for (int i0s = 0; i0s < n; i0s += 32) {
             const int i = i0s + lane;
             const bool valid = i < n;
@@ -544,18 +562,75 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
             const float ey = fmaxf(fmaxf(loy - a.y, a.y - hiy), 0.0f);
             const float ez = fmaxf(fmaxf(loz - a.z, a.z - hiz), 0.0f);
             const bool near = fmaf(ez, ez, fmaf(ey, ey, ex * ex)) < p.cull2;
-            const unsigned m = __ballot_sync(0xffffffffu, near);
-            if (near && CP_IN(cnt + __popc(m & below), kStageAtoms, p.status))
-                list[cnt + __popc(m & below)] = REL ? make_float4(p.ox - a.x, p.oy - a.y, p.oz - a.z, a.w) : a;
-            cnt += __popc(m);
+            // the sub-box's point farthest from the atom is one of its corners
+            const float fx = fmaxf(a.x - lox, hix - a.x), fy = fmaxf(a.y - loy, hiy - a.y);
+            const float fz = fmaxf(a.z - loz, hiz - a.z);
+            const bool whole = near && fmaf(fz, fz, fmaf(fy, fy, fx * fx)) < p.c2;
+            const unsigned mf = __ballot_sync(0xffffffffu, whole);
+            const unsigned mp = __ballot_sync(0xffffffffu, near && !whole);
+            const float4 entry = REL ? make_float4(p.ox - a.x, p.oy - a.y, p.oz - a.z, a.w) : a;
+            if (whole && CP_IN(cnt_f + __popc(mf & below), kStageAtoms, p.status))
+                list[cnt_f + __popc(mf & below)] = entry;
+            if (near && !whole && CP_IN(kStageAtoms - 1 - cnt_p - __popc(mp & below), kStageAtoms, p.status))
+                list[kStageAtoms - 1 - cnt_p - __popc(mp & below)] = entry;
+            cnt_f += __popc(mf);
+            cnt_p += __popc(mp);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled: the list holds copies
-        if (COUNT) n_near += (unsigned)cnt;
-        // (2) every listed atom against the lane's 4 points
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        if (COUNT) n_near += (unsigned)(cnt_f + cnt_p);
+        // (2) the full atoms' moments, lane t taking atoms t, t + 32, ...
+        for (int t = lane; t < cnt_f && !COUNT; t += 32) {
+            const float4 e = list[t];
+            const float wx = REL ? -e.x - cx : e.x - cx;
+            const float wy = REL ? -e.y - cy : e.y - cy;
+            const float wz = REL ? -e.z - cz : e.z - cz;
+            const float m = fmaf(wz, wz, fmaf(wy, wy, wx * wx));
+            const float qm = e.w * m, qx = e.w * wx, qy = e.w * wy, qz = e.w * wz;
+            mq += e.w;
+            mqx += qx;
+            mqy += qy;
+            mqz += qz;
+            mqm += qm;
+            mqmm = fmaf(qm, m, mqmm);
+            mrx = fmaf(qm, wx, mrx);
+            mry = fmaf(qm, wy, mry);
+            mrz = fmaf(qm, wz, mrz);
+            mtxx = fmaf(qx, wx, mtxx);
+            mtxy = fmaf(qx, wy, mtxy);
+            mtxz = fmaf(qx, wz, mtxz);
+            mtyy = fmaf(qy, wy, mtyy);
+            mtyz = fmaf(qy, wz, mtyz);
+            mtzz = fmaf(qz, wz, mtzz);
+        }
+        // (3) every listed atom against the lane's 4 points.  Full atoms add
+        // q / r only (their -q g(r) is in the moments); partial atoms add the
+        // switched term where r < c.
+        float2 pf01 = make_float2(0.f, 0.f), pf23 = make_float2(0.f, 0.f);
 #pragma unroll 2
-        for (int t = 0; t < cnt; ++t) {
+        for (int t = 0; t < cnt_f; ++t) {
+            const float4 a = list[t];  // broadcast
+            const float dy = diff(y, a.y), dz = diff(z, a.z);
+            const float d = fmaf(dy, dy, dz * dz);
+            const float2 dyz2 = make_float2(d, d);
+            const float2 dx01 = make_float2(diff(x[0], a.x), diff(x[1], a.x));
+            const float2 dx23 = make_float2(diff(x[2], a.x), diff(x[3], a.x));
+            const float2 r01 = __ffma2_rn(dx01, dx01, dyz2);
+            const float2 r23 = __ffma2_rn(dx23, dx23, dyz2);
+            const float2 rs01 = make_float2(sfu_rsqrt(r01.x), sfu_rsqrt(r01.y));
+            const float2 rs23 = make_float2(sfu_rsqrt(r23.x), sfu_rsqrt(r23.y));
+            const float2 qq = make_float2(a.w, a.w);
+            pf01 = __ffma2_rn(qq, rs01, pf01);
+            pf23 = __ffma2_rn(qq, rs23, pf23);
+            if (COUNT) {
+                const float r2c[4] = {r01.x, r01.y, r23.x, r23.y};
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (r2c[c] < p.c2 && i0 + c < p.nx && j < p.ny && k < p.nz) ++n_useful;
+            }
+        }
+#pragma unroll 2
+        for (int t = kStageAtoms - cnt_p; t < kStageAtoms; ++t) {
             const float4 a = list[t];  // broadcast
             // differences as scalars (dy^2 + dz^2 is the same for the
             // lane's 4 points), written into the f32x2 operand pairs
@@ -571,10 +646,10 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
             const float2 rs23 = make_float2(sfu_rsqrt(r23.x), sfu_rsqrt(r23.y));
             const float2 e01 = __fadd2_rn(rs01, __ffma2_rn(__ffma2_rn(r01, NG2, NG1), r01, NG0));
             const float2 e23 = __fadd2_rn(rs23, __ffma2_rn(__ffma2_rn(r23, NG2, NG1), r23, NG0));
-            if (r01.x < p.c2) part[0] = fmaf(a.w, e01.x, part[0]);
-            if (r01.y < p.c2) part[1] = fmaf(a.w, e01.y, part[1]);
-            if (r23.x < p.c2) part[2] = fmaf(a.w, e23.x, part[2]);
-            if (r23.y < p.c2) part[3] = fmaf(a.w, e23.y, part[3]);
+            if (r01.x < p.c2) pf01.x = fmaf(a.w, e01.x, pf01.x);
+            if (r01.y < p.c2) pf01.y = fmaf(a.w, e01.y, pf01.y);
+            if (r23.x < p.c2) pf23.x = fmaf(a.w, e23.x, pf23.x);
+            if (r23.y < p.c2) pf23.y = fmaf(a.w, e23.y, pf23.y);
             if (COUNT) {
                 const float r2c[4] = {r01.x, r01.y, r23.x, r23.y};
 #pragma unroll
@@ -582,9 +657,53 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
                     if (r2c[c] < p.c2 && i0 + c < p.nx && j < p.ny && k < p.nz) ++n_useful;
             }
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[c] += part[c];
+        acc[0] += pf01.x;
+        acc[1] += pf01.y;
+        acc[2] += pf23.x;
+        acc[3] += pf23.y;
         __syncwarp();  // the list is rewritten by the next stage
+    }
+
+    // -sum over the full atoms of q g(r) at each of the lane's points, from
+    // the moments: with u = point - centre, r^2 = s - 2 u.w + m (s = |u|^2),
+    //   sum q r^2 = s Q - 2 u.Q1 + M,
+    //   sum q r^4 = s (s Q + 2 M - 4 u.Q1) + M2 - 4 u.R + 4 u^T T u,
+    // and -g(r) = NG0 + NG1 r^2 + NG2 r^4.
+#pragma unroll
+    for (int o = 16; o > 0 && !COUNT; o >>= 1) {
+        mq += __shfl_xor_sync(0xffffffffu, mq, o);
+        mqx += __shfl_xor_sync(0xffffffffu, mqx, o);
+        mqy += __shfl_xor_sync(0xffffffffu, mqy, o);
+        mqz += __shfl_xor_sync(0xffffffffu, mqz, o);
+        mqm += __shfl_xor_sync(0xffffffffu, mqm, o);
+        mqmm += __shfl_xor_sync(0xffffffffu, mqmm, o);
+        mrx += __shfl_xor_sync(0xffffffffu, mrx, o);
+        mry += __shfl_xor_sync(0xffffffffu, mry, o);
+        mrz += __shfl_xor_sync(0xffffffffu, mrz, o);
+        mtxx += __shfl_xor_sync(0xffffffffu, mtxx, o);
+        mtxy += __shfl_xor_sync(0xffffffffu, mtxy, o);
+        mtxz += __shfl_xor_sync(0xffffffffu, mtxz, o);
+        mtyy += __shfl_xor_sync(0xffffffffu, mtyy, o);
+        mtyz += __shfl_xor_sync(0xffffffffu, mtyz, o);
+        mtzz += __shfl_xor_sync(0xffffffffu, mtzz, o);
+    }
+    if (!COUNT) {
+        const float uy = REL ? fmaf(y, p.h, -cy) : y - cy;
+        const float uz = REL ? fmaf(z, p.h, -cz) : z - cz;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float ux = REL ? fmaf(x[c], p.h, -cx) : x[c] - cx;
+            const float su = fmaf(uz, uz, fmaf(uy, uy, ux * ux));
+            const float uq = fmaf(uz, mqz, fmaf(uy, mqy, ux * mqx));
+            const float ur = fmaf(uz, mrz, fmaf(uy, mry, ux * mrx));
+            const float tx = fmaf(uz, mtxz, fmaf(uy, mtxy, ux * mtxx));
+            const float ty = fmaf(uz, mtyz, fmaf(uy, mtyy, ux * mtxy));
+            const float tz = fmaf(uz, mtzz, fmaf(uy, mtyz, ux * mtxz));
+            const float utu = fmaf(uz, tz, fmaf(uy, ty, ux * tx));
+            const float s2 = fmaf(su, mq, fmaf(-2.f, uq, mqm));
+            const float s4 = fmaf(su, fmaf(su, mq, fmaf(2.f, mqm, -4.f * uq)), fmaf(4.f, utu, fmaf(-4.f, ur, mqmm)));
+            acc[c] += fmaf(NG2.x, s4, fmaf(NG1.x, s2, NG0.x * mq));
+        }
     }
 
     if (COUNT) {
