@@ -63,7 +63,7 @@ def env_rank():
     return rank, world, local
 
 
-def config_dict(wd, wc, capacity):
+def config_dict(wd, wc, capacity, shards=0):
     return {
         "workload": f"direct {wd.shape[0]}x{wd.shape[1]}x{wd.shape[2]} grid, {wd.n_atoms} clustered atoms, "
         f"h={wd.h} A (config {CONFIG_NUMBER.get(wd.meta.get('key', ''), '?')}); "
@@ -77,8 +77,19 @@ def config_dict(wd, wc, capacity):
                    "bin_size": wc.bin_size, "capacity": capacity, "brick": [8, 8, 8],
                    "description": wc.description},
         "l2": "flushed before every timed launch (256 MiB write)",
-        "parallelism": "one independent copy per rank (weak scaling)",
+        "parallelism": (f"one map shared by {shards} ranks as z-slabs, each rank all atoms (strong scaling)"
+                        if shards else "one independent copy per rank (weak scaling)"),
     }
+
+
+def slab_workload(w, rank, world, align):
+    """The rank's z-slab of workload `w` (same atoms, the slab's grid)."""
+    import dataclasses
+
+    from direct_coulomb_summation_gb300 import shard
+
+    _, shape, origin = shard.slab_grid(w.shape, w.origin, w.h, rank, world, align)
+    return dataclasses.replace(w, shape=shape, origin=origin, meta=dict(w.meta))
 
 
 def make_workload(name):
@@ -101,6 +112,18 @@ def max_over_ranks(values, device=None):
         return list(values)
     t = torch.tensor(values, dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+def sum_over_ranks(values, device=None):
+    """Elementwise sum of a list of numbers over all ranks (identity at world size 1)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return t.cpu().tolist()
 
 
@@ -408,8 +431,17 @@ def run_ours(args):
     props = torch.cuda.get_device_properties(device)
     n_sm = props.multi_processor_count
 
-    wd = make_workload(args.direct_workload)
-    wc = make_workload(args.cutoff_workload)
+    wd_full = make_workload(args.direct_workload)
+    wc_full = make_workload(args.cutoff_workload)
+    wd, wc = wd_full, wc_full
+    if args.shard_map:
+        # strong scaling: the ranks share one map, each computing a z-slab
+        wd = slab_workload(wd_full, rank, world, 1)
+        wc = slab_workload(wc_full, rank, world, 8)
+        if wd.shape[2] == 0 or wc.shape[2] == 0:
+            raise RuntimeError("--shard-map: more ranks than slabs")
+    # how many full workloads one timed step covers, over all ranks
+    job = 1 if args.shard_map else world
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
 
@@ -450,6 +482,10 @@ def run_ours(args):
         counts = cp.cutoff_pair_counts(ac, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity,
                                        workspace=ws)
         stats = cp.cutoff_stats(ws, wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity)
+        if args.shard_map:  # the whole map's pairs: every rank's slab
+            counts = dict(zip(("useful", "evaluated", "examined"),
+                              (int(v) for v in sum_over_ranks([counts["useful"], counts["evaluated"],
+                                                               counts["examined"]], device))))
 
     sampler = ClockSampler(gpu_id_for(torch, device))
     for _ in range(args.warmup):
@@ -511,9 +547,11 @@ def run_ours(args):
         [t_direct, t_bin, t_map, t_wall, med_direct, med_cut, med_map, med_bin], device)
     t_direct, t_bin, t_map = (max(t, 1e-12) for t in (t_direct, t_bin, t_map))
     K = args.steps
-    direct_rate = float(wd.n_pairs) * world * K / t_direct
+    # counts are the whole map's in --shard-map mode, one rank's otherwise
+    cmul = 1 if args.shard_map else world
+    direct_rate = float(wd_full.n_pairs) * job * K / t_direct
     t_cut = t_bin + t_map
-    points_rate = float(wc.n_points) * world * K / t_cut
+    points_rate = float(wc_full.n_points) * job * K / t_cut
 
     f_mhz = clocks.get("sm_mhz") or 2070.0
     clock_basis = "median SM clock sampled during the timed steps" if clocks.get("sm_mhz") else "max SM clock"
@@ -558,7 +596,7 @@ def run_ours(args):
         sec_sampler = ClockSampler(gpu_id_for(torch, device))
         sec_sampler.mark_begin()
         secondary = measure_secondary(cp, lib, torch, device, stream, flush, roof, hbm_peak, hbm_basis,
-                                      do_direct, do_cutoff, args.capacity, {args.cutoff_workload: wc})
+                                      do_direct, do_cutoff, args.capacity, {args.cutoff_workload: wc_full})
         sec_sampler.mark_end()
         secondary["clocks"] = sec_sampler.stop()
 
@@ -583,6 +621,21 @@ def run_ours(args):
                                      n_e2e, args.capacity, do_direct, do_cutoff)
         t_e2e_d, t_e2e_c = max_over_ranks([t_e2e_d, t_e2e_c], device)
 
+    # --shard-map: the gather of the slabs to rank 0 (after the steps, timed once)
+    gather = None
+    if args.shard_map and world > 1:
+        from direct_coulomb_summation_gb300 import shard
+
+        gather = {}
+        for key, V, w, align in (("direct", Vd, wd_full, 1), ("cutoff", Vc, wc_full, 8)):
+            barrier(device)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            shard.gather_slabs(V, w.shape, align, dst=0)
+            torch.cuda.synchronize()
+            gather["ms_" + key] = max_over_ranks([1e3 * (time.perf_counter() - t0)], device)[0]
+        gather["bytes"] = {"direct": wd_full.n_points * 4, "cutoff": wc_full.n_points * 4}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -592,9 +645,9 @@ def run_ours(args):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         threads = host_threads()
-        rate, n_pts, dt = oracle_direct_rate(wd, args.cpu_seconds, threads)
-        crate, c_pts, cdt = oracle_cutoff_rate(wc, args.cpu_seconds / 2, threads)
-        srate, s_pts, sdt = oracle_direct_rate(wd, args.cpu_seconds / 4, 1)
+        rate, n_pts, dt = oracle_direct_rate(wd_full, args.cpu_seconds, threads)
+        crate, c_pts, cdt = oracle_cutoff_rate(wc_full, args.cpu_seconds / 2, threads)
+        srate, s_pts, sdt = oracle_direct_rate(wd_full, args.cpu_seconds / 4, 1)
         cpu = {"value": rate, "unit": "pair evals/s", "cores": threads, "kind": "oracle",
                "sample": f"fp64 direct sum at {n_pts} seeded grid points of the {tuple(wd.shape)} grid x "
                          f"{wd.n_atoms} atoms ({dt:.1f} s)",
@@ -609,7 +662,7 @@ def run_ours(args):
     traffic_map = traffic_from_profile("cutoff_brick_kernel", "direct_coulomb_summation_gb300/csrc/cp_cutoff.cu",
                                        args.cutoff_workload)
     rd = roof.direct(direct_rate, world)
-    useful_rate = counts["useful"] * world * K / t_map
+    useful_rate = counts["useful"] * cmul * K / t_map
     L = cp.cutoff_layout(wc.n_atoms, wc.shape, wc.origin, wc.h, wc.cutoff, wc.bin_size, args.capacity)
     bin_bytes = bin_bytes_of(L, wc.n_atoms, args.capacity)
     line = {
@@ -621,11 +674,11 @@ def run_ours(args):
         "warmup": args.warmup,
         "ms_per_step": 1e3 * (t_direct + t_cut) / K,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if args.shard_map else "weak",
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": config_dict(wd, wc, args.capacity),
+        "config": config_dict(wd_full, wc_full, args.capacity, world if args.shard_map else 0),
         "roofline": {
             "bound": "alu",
             "kernel": "direct_kernel (cp_direct)",
@@ -649,7 +702,7 @@ def run_ours(args):
         "direct": {
             "config": CONFIG_NUMBER.get(args.direct_workload),
             "pair_evals_per_s": direct_rate,
-            "grid_points_per_s": float(wd.n_points) * world * K / t_direct,
+            "grid_points_per_s": float(wd_full.n_points) * job * K / t_direct,
             "ms": 1e3 * t_direct / K,
             "ms_median": med_direct if do_direct else None,
             "plan": list(cp.direct_plan(wd.n_atoms, wd.shape)),
@@ -658,9 +711,9 @@ def run_ours(args):
             "config": CONFIG_NUMBER.get(args.cutoff_workload),
             "capacity": args.capacity,
             "grid_points_per_s": points_rate,
-            "useful_pairs_per_s": counts["useful"] * world * K / t_cut,
-            "evaluated_pairs_per_s": counts["evaluated"] * world * K / t_cut,
-            "examined_pairs_per_s": counts["examined"] * world * K / t_cut,
+            "useful_pairs_per_s": counts["useful"] * cmul * K / t_cut,
+            "evaluated_pairs_per_s": counts["evaluated"] * cmul * K / t_cut,
+            "examined_pairs_per_s": counts["examined"] * cmul * K / t_cut,
             "pairs_per_step": counts,
             "evaluated_per_useful": counts["evaluated"] / counts["useful"] if counts["useful"] else None,
             "binning_stats": stats,
@@ -682,22 +735,23 @@ def run_ours(args):
                            f"FFMA {r_ffma:.1f}/11) x {f_mhz:.0f} MHz",
                 tight_basis=f"min(SFU {r_mufu:.2f}, 128 issue/8) = {roof.useful_tight:.1f} useful pairs/clk/SM"),
             "roofline_binning": {
-                "bound": "hbm", "achieved": bin_bytes * world * K / t_bin / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                "frac": bin_bytes * world * K / t_bin / 1e9 / hbm_peak,
+                "bound": "hbm", "achieved": bin_bytes * world * K / t_bin / 1e9, "peak": hbm_peak * world,
+                "unit": "GB/s", "frac": bin_bytes * K / t_bin / 1e9 / hbm_peak,
                 "traffic": traffic_from_profile("binning", "direct_coulomb_summation_gb300/csrc/cp_cutoff.cu",
                                                 args.cutoff_workload),
                 "algorithmic_bytes": bin_bytes, "peak_basis": f"hbm_gbs {hbm_basis}",
             },
         },
         "secondary": secondary,
+        "shard_gather": gather,
         "msm": msm,
         "cpu_baseline": cpu,
         "e2e": {
-            "value": float(wd.n_pairs) * world / t_e2e_d,
+            "value": float(wd_full.n_pairs) * job / t_e2e_d,
             "unit": "pair evals/s",
             "h2d_bytes_per_step": int(wd.atoms.nbytes),
             "d2h_bytes_per_step": int(Vd.numel() * 4),
-            "cutoff_grid_points_per_s": float(wc.n_points) * world / t_e2e_c,
+            "cutoff_grid_points_per_s": float(wc_full.n_points) * job / t_e2e_c,
             "cutoff_h2d_bytes": int(wc.atoms.nbytes),
             "cutoff_d2h_bytes": int(Vc.numel() * 4),
             "how": "public Python API with pinned host atoms in, host V out; wall clock per call incl. copies",
@@ -954,6 +1008,8 @@ def main(argv=None):
     ap.add_argument("--only", choices=["both", "direct", "cutoff"], default="both",
                     help="time one leg only (for profiling; the JSON line then covers that leg)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--shard-map", action="store_true",
+                    help="the ranks share one map as z-slabs (strong scaling) instead of one copy each")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the per-workload timings after the steps (for profiling)")
     ap.add_argument("--direct-workload", choices=["direct_plane", "direct_3d", "direct_protein"], default=DIRECT_WL,

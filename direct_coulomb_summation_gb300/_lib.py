@@ -103,6 +103,7 @@ SIGNATURES = {
     "cp_msm_longrange": (_I, [_P, _I, *_GRID, cp_vec3, cp_vec3, _F, _F, _P, _SZ, _P, _I, _P]),
     "cp_atom_bounds": (_I, [_P, _I, _P, _P]),
     "cp_probe_wait_timeout": (_I, [ctypes.c_ulonglong, _P, _P]),
+    "cp_slab": (_I, [_I, _I, _I, _I, _F, _F, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_F)]),
 }
 
 

@@ -307,6 +307,23 @@ CP_API const char *cp_status_string(int status) {
 
 CP_API int cp_version(void) { return 100; }
 
+CP_API int cp_slab(int nz, int world, int rank, int align, float origin_z, float h, int *z0, int *nz_slab,
+                   float *origin_z_slab) {
+    if (nz < 1 || world < 1 || rank < 0 || rank >= world || align < 1 || !z0 || !nz_slab || !origin_z_slab ||
+        !std::isfinite(origin_z) || !std::isfinite(h) || !(h > 0.0f))
+        return CP_ERR_INVALID_ARGUMENT;
+    // whole units of `align` planes, split as evenly as integer division
+    // allows, in rank order; the last unit may be cut short by nz
+    const long long units = ((long long)nz + align - 1) / align;
+    const long long u0 = units * rank / world, u1 = units * (rank + 1) / world;
+    const long long p0 = std::min<long long>(u0 * align, nz), p1 = std::min<long long>(u1 * align, nz);
+    *z0 = (int)p0;
+    *nz_slab = (int)(p1 - p0);
+    // the full grid's plane z0, formed as the kernels form a grid coordinate
+    *origin_z_slab = fmaf((float)p0, h, origin_z);
+    return CP_OK;
+}
+
 CP_API unsigned long long cp_launch_count(void) { return cpmap::launch_count(); }
 
 CP_API int cp_cutoff_layout_of(int n_atoms, int nx, int ny, int nz, cp_vec3 origin, float h, float cutoff,

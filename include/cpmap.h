@@ -445,6 +445,30 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
 CP_API int cp_atom_bounds(const float *atoms, int n_atoms, float *bounds, void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Sharding a map over several GPUs by z-slabs (PMPP ch.18 notes, sections
+ * 18.2 and 18.5: grid points are independent -- each is written only by the
+ * thread that owns it -- so a map splits into slabs of planes that separate
+ * GPUs compute with no exchange; the direct sum needs every atom on every
+ * GPU, the cutoff sum only the atoms within c of a slab, which the bin rule
+ * of the slab's own grid selects by itself).
+ *
+ * Host-only.  Rank `rank` of `world` owns planes z0 .. z0 + *nz_slab - 1 of
+ * a grid of nz planes: the planes are cut into units of `align` planes (8
+ * keeps the cutoff map's 8x8x8-point bricks whole), the units are shared
+ * out as evenly as integer division allows, in rank order, and the last
+ * unit may be cut short by nz.  A rank past the last unit gets
+ * *nz_slab = 0.  *origin_z_slab = fmaf(z0, h, origin_z), the full grid's
+ * plane z0 formed as the kernels form a grid coordinate, so that the slab
+ * grid (nx, ny, *nz_slab; origin (x, y, *origin_z_slab); h) has exactly the
+ * full grid's points when those are fp32 numbers (cp_grid_points_exact).
+ * Calling cp_direct / cp_cutoff on the slab grid with V pointing at plane
+ * z0 of the full map computes that slab.  Returns CP_OK or
+ * CP_ERR_INVALID_ARGUMENT (nz, world or align below 1, rank outside
+ * [0, world), a null pointer, non-finite origin_z or h <= 0).              */
+CP_API int cp_slab(int nz, int world, int rank, int align, float origin_z, float h, int *z0, int *nz_slab,
+                   float *origin_z_slab);
+
+/* ------------------------------------------------------------------------ */
 /* Status and measurement helpers. */
 
 /* Reads and clears the device status word of the current device

@@ -26,8 +26,9 @@ def _rank_main(rank, world, port, out):
     dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
     mine = [1.0 + rank, 10.0 - rank, 3.5]
     got = bench.max_over_ranks(mine)
+    total = bench.sum_over_ranks([1.0 + rank, 2.0])
     bench.barrier()
-    out.put((rank, got))
+    out.put((rank, (got, total)))
     dist.destroy_process_group()
 
 
@@ -44,7 +45,7 @@ def test_max_over_ranks_gloo():
         p.join(timeout=60)
         assert p.exitcode == 0
     for r in range(world):
-        assert res[r] == [2.0, 10.0, 3.5]
+        assert res[r] == ([2.0, 10.0, 3.5], [3.0, 4.0])
 
 
 def test_max_over_ranks_single_process_is_identity():
@@ -73,3 +74,21 @@ def test_clock_samples_that_invalidate_a_run():
     assert bench.clocks_rejected(dict(ok, sm_mhz=1200.0))  # stuck low with no reason: a clock lock
     assert not bench.clocks_rejected(dict(ok, sm_mhz=1200.0, reasons=["sw_power_cap"]))
     assert not bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]})
+
+
+def test_shard_map_slab_workloads_cover_the_grid():
+    """--shard-map: the ranks' slab workloads hold all atoms and together
+    exactly the full grid's planes, cutoff slabs in whole 8-plane bricks."""
+    import workloads
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    w = workloads.make("cutoff_uniform")
+    for world in (1, 2, 3, 4):
+        slabs = [bench.slab_workload(w, r, world, 8) for r in range(world)]
+        assert sum(s.shape[2] for s in slabs) == w.shape[2]
+        for s in slabs:
+            assert s.shape[:2] == w.shape[:2] and s.atoms is w.atoms
+        zs = [round((s.origin[2] - w.origin[2]) / w.h) for s in slabs]
+        assert zs == sorted(zs) and all(z % 8 == 0 for z in zs)
