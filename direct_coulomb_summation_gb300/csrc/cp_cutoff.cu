@@ -606,8 +606,10 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
         // (3) every listed atom against the lane's 4 points.  Full atoms add
         // q / r only (their -q g(r) is in the moments); partial atoms add the
         // switched term where r < c.
+        // (both loops unrolled by 8: 4 % faster than by 2 on the 200^3 and
+        // 400^3 maps, the most of 1, 2, 3, 4 and 8)
         float2 pf01 = make_float2(0.f, 0.f), pf23 = make_float2(0.f, 0.f);
-#pragma unroll 2
+#pragma unroll 8
         for (int t = 0; t < cnt_f; ++t) {
             const float4 a = list[t];  // broadcast
             const float dy = diff(y, a.y), dz = diff(z, a.z);
@@ -629,7 +631,7 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
                     if (r2c[c] < p.c2 && i0 + c < p.nx && j < p.ny && k < p.nz) ++n_useful;
             }
         }
-#pragma unroll 2
+#pragma unroll 8
         for (int t = kStageAtoms - cnt_p; t < kStageAtoms; ++t) {
             const float4 a = list[t];  // broadcast
             // differences as scalars (dy^2 + dz^2 is the same for the
