@@ -890,6 +890,9 @@ def measure_msm(cp, lib, torch, device, stream, flush, args, roof, call):
         call(lib.cp_msm_longrange(a.data_ptr(), w.n_atoms, *g, *dom, cut[0], h0, mws.data_ptr(),
                                   int(ML.total_bytes), V.data_ptr(), 1, sh), "cp_msm_longrange")
 
+    c_launch0 = lib.cp_launch_count()
+    run_cut()
+    launches_cut = lib.cp_launch_count() - c_launch0
     m_launch0 = lib.cp_launch_count()
     tc, tm = _timed_runs(torch, stream, flush, [run_cut, run_msm], reps=max(3, min(args.steps, 20)))
     n_calls = 3 + max(3, min(args.steps, 20))
@@ -899,7 +902,6 @@ def measure_msm(cp, lib, torch, device, stream, flush, args, roof, call):
     # below the top times the stencil's taps, plus the dense top level
     fma = sum(nodes[:-1]) * int(ML.taps) + nodes[-1] ** 2
     ms_l, ms_c = float(np.median(tm)), float(np.median(tc))
-    launches_cut = 7
     return {"workload": w.description, "lattice_h": h0, "levels": levels, "nodes": nodes,
             "stencil_taps": int(ML.taps), "ms_longrange": ms_l,
             "launches_per_call": int((lib.cp_launch_count() - m_launch0) // n_calls - launches_cut),

@@ -5,12 +5,17 @@
 // Overfull Bins" (34); PMPP ch.18 notes section 18.5 BinTable) runs on the
 // GPU as a counting sort:
 //   clear -> count (atomic per-bin counters, each atom keeps its arrival
-//   rank) -> exclusive scan (per-block scans + one scan of block sums) ->
-//   scatter (input index to bin-sorted position) -> per-bin sort by input
-//   index (one warp per bin, rank by comparison) and pack: the first K atoms
-//   of each bin into its fixed-capacity slots, every atom into the
-//   bin-sorted (CSR) array.  Results are deterministic: within a bin the
-//   order is ascending input index whatever order the atomics ran in.
+//   rank) -> exclusive scan (per-block scans; the scan of the block sums
+//   runs in the scatter kernel's prologue when there are at most 1024
+//   blocks, else in a launch of its own) -> scatter (input index to
+//   bin-sorted position) -> per-bin sort by input index (one warp per bin,
+//   rank by comparison) and pack: the first K atoms of each bin into its
+//   fixed-capacity slots, every atom into the bin-sorted (CSR) array.
+//   Results are deterministic: within a bin the order is ascending input
+//   index whatever order the atomics ran in.  Every launch, and the brick
+//   kernel's after them, is a programmatic dependent launch: it may be
+//   scheduled while the one before it drains, and waits for it
+//   (griddepcontrol.wait) before touching memory.
 //
 // The map (slides "Details on Small Bin Design" (30), "Tiling Atom Data"
 // (32), "GPU Thread Coarsening" (36), "GPU Thread Inner Loop" (37)): one CTA
@@ -69,8 +74,13 @@ struct BinParams {
     int2 *bin_rank;
     int *block_sums;
     int *block_prefix;
+    int prefix_inline;     // > 0: the scatter kernel scans this many block totals itself
     unsigned int *status;  // checked build: index checks record here
 };
+
+// Largest number of block totals the scatter kernel scans in its prologue
+// (instead of a separate one-CTA launch).
+constexpr int kInlinePrefixMax = 1024;
 
 // fp32 bin coordinate: floor(float(float(a - bo) / b)), -1 outside [0, nb)
 // (NaN fails both comparisons).
@@ -82,12 +92,16 @@ __device__ __forceinline__ int bin_axis(float a, float bo, float b, int nb) {
 }
 
 __global__ void bin_clear_kernel(const __grid_constant__ BinParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.nbins; i += stride) p.count[i] = 0;
     if (blockIdx.x == 0 && threadIdx.x < 8) p.stats[threadIdx.x] = 0;
 }
 
 __global__ void bin_count_kernel(const __grid_constant__ BinParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= p.n) return;
     const float4 a = p.atoms[i];
@@ -107,6 +121,8 @@ __global__ void bin_count_kernel(const __grid_constant__ BinParams p) {
 // Exclusive scan of count within blocks of kScanBlock bins (256 threads x 8);
 // local results go to start[], block totals to block_sums[].
 __global__ void __launch_bounds__(256) bin_scan_local_kernel(const __grid_constant__ BinParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int warp_tot[8];
     const int base = blockIdx.x * kScanBlock + threadIdx.x * 8;
     int v[8];
@@ -143,6 +159,8 @@ __global__ void __launch_bounds__(256) bin_scan_local_kernel(const __grid_consta
 // One CTA: exclusive scan of the block totals; also start[nbins] and the
 // binned-atom count.
 __global__ void __launch_bounds__(1024) bin_scan_blocks_kernel(const __grid_constant__ BinParams p, int nblk) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int warp_tot[32];
     const int base = threadIdx.x * 8;
     int v[8];
@@ -179,11 +197,45 @@ __global__ void __launch_bounds__(1024) bin_scan_blocks_kernel(const __grid_cons
 }
 
 __global__ void bin_scatter_kernel(const __grid_constant__ BinParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ int pre[kInlinePrefixMax];
+    const int nblk = p.prefix_inline;
+    if (nblk > 0) {
+        // the exclusive prefix of the block totals, by warp 0 (each lane a
+        // run of consecutive totals, then a shuffle scan of the run sums);
+        // block 0 also stores it, start[nbins] and the binned count
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            const int per = (nblk + 31) / 32;
+            const int b0 = min(lane * per, nblk), b1 = min(b0 + per, nblk);
+            int sum = 0;
+            for (int b = b0; b < b1; ++b) sum += p.block_sums[b];
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            int run = incl - sum;
+            for (int b = b0; b < b1; ++b) {
+                pre[b] = run;
+                if (blockIdx.x == 0) p.block_prefix[b] = run;
+                run += p.block_sums[b];
+            }
+            if (blockIdx.x == 0 && lane == 31) {
+                p.start[p.nbins] = incl;
+                p.stats[0] = incl;
+            }
+        }
+        __syncthreads();
+    }
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= p.n) return;
     const int2 br = p.bin_rank[i];
     if (br.x < 0) return;
-    const int pos = p.start[br.x] + p.block_prefix[br.x / kScanBlock] + br.y;
+    const int blk = br.x / kScanBlock;
+    const int pos = p.start[br.x] + (nblk > 0 ? pre[blk] : p.block_prefix[blk]) + br.y;
     if (CP_IN(pos, p.n, p.status)) p.csr_index[pos] = i;
 }
 
@@ -191,6 +243,8 @@ __global__ void bin_scatter_kernel(const __grid_constant__ BinParams p) {
 // bin-sorted atoms and indices and the fixed-capacity slots (pads after the
 // last atom), and the final start[] entry.  8 bins per 256-thread block.
 __global__ void __launch_bounds__(256) bin_sort_pack_kernel(const __grid_constant__ BinParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int blk_overflow, blk_max;
     if (threadIdx.x == 0) {
         blk_overflow = 0;
@@ -245,6 +299,8 @@ __global__ void __launch_bounds__(256) bin_sort_pack_kernel(const __grid_constan
 constexpr int kLaneSortMax = 16;
 
 __global__ void __launch_bounds__(256) bin_sort_pack_lane_kernel(const __grid_constant__ BinParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int blk_overflow, blk_max;
     if (threadIdx.x == 0) {
         blk_overflow = 0;
@@ -367,6 +423,8 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
     __shared__ uint64_t full[kBrickStages], empty[kBrickStages];
     __shared__ volatile int stage_n[kBrickStages];
 
+    pdl_launch_dependents();
+    pdl_wait();  // binning's results
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int brick = blockIdx.x;
     const int bx = brick % p.nbr[0];
@@ -745,6 +803,25 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
 
 namespace {
 
+// Launches kernel<<<grid, block, 0, stream>>>(args...) with programmatic
+// stream serialization: it may be scheduled while the previous kernel on
+// the stream drains, and it waits for that kernel (pdl_wait) before
+// touching memory.
+template <typename... KArgs, typename... Args>
+bool launch_pdl(void (*kernel)(KArgs...), int grid, int block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess;
+}
+
 // Kernel arguments of the binning kernels for the sections of `L` at `ws`.
 BinParams bin_params(const float4 *atoms, int n_atoms, const BinGeom &bg, const cp_cutoff_layout &L, void *workspace) {
     char *ws = static_cast<char *>(workspace);
@@ -772,6 +849,7 @@ BinParams bin_params(const float4 *atoms, int n_atoms, const BinGeom &bg, const 
     b.block_sums = reinterpret_cast<int *>(ws + off);
     off += (4 * nblk + 255) & ~(size_t)255;
     b.block_prefix = reinterpret_cast<int *>(ws + off);
+    b.prefix_inline = 0;
     b.status = device_status_ptr();
     return b;
 }
@@ -782,17 +860,24 @@ int launch_binning_params(const BinParams &b, cudaStream_t stream, bool small_bi
     int rc = device_info(&dev);
     if (rc) return rc;
     const int clear_blocks = (int)std::min<long long>((b.nbins + 255) / 256, 8LL * dev.sm_count);
-    bin_clear_kernel<<<std::max(clear_blocks, 1), 256, 0, stream>>>(b);
-    if (b.n > 0) bin_count_kernel<<<(b.n + 255) / 256, 256, 0, stream>>>(b);
-    bin_scan_local_kernel<<<nblk, 256, 0, stream>>>(b);
-    bin_scan_blocks_kernel<<<1, 1024, 0, stream>>>(b, nblk);
-    if (b.n > 0) bin_scatter_kernel<<<(b.n + 255) / 256, 256, 0, stream>>>(b);
+    // each launch may be scheduled while the one before it drains (the
+    // kernels wait for it before touching memory)
+    bool ok = launch_pdl(bin_clear_kernel, std::max(clear_blocks, 1), 256, stream, b);
+    if (b.n > 0) ok = ok && launch_pdl(bin_count_kernel, (b.n + 255) / 256, 256, stream, b);
+    ok = ok && launch_pdl(bin_scan_local_kernel, nblk, 256, stream, b);
+    // up to kInlinePrefixMax block totals the scatter kernel scans itself
+    const bool inline_prefix = b.n > 0 && nblk <= kInlinePrefixMax;
+    BinParams bs = b;
+    bs.prefix_inline = inline_prefix ? nblk : 0;
+    if (!inline_prefix) ok = ok && launch_pdl(bin_scan_blocks_kernel, 1, 1024, stream, b, nblk);
+    if (b.n > 0) ok = ok && launch_pdl(bin_scatter_kernel, (b.n + 255) / 256, 256, stream, bs);
     if (small_bins)
-        bin_sort_pack_lane_kernel<<<(b.nbins + 255) / 256, 256, 0, stream>>>(b);
+        ok = ok && launch_pdl(bin_sort_pack_lane_kernel, (int)((b.nbins + 255) / 256), 256, stream, b);
     else
-        bin_sort_pack_kernel<<<(b.nbins + 7) / 8, 256, 0, stream>>>(b);
+        ok = ok && launch_pdl(bin_sort_pack_kernel, (int)((b.nbins + 7) / 8), 256, stream, b);
+    if (!ok) return CP_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
-    note_launches(b.n > 0 ? 6 : 4);
+    note_launches(b.n > 0 ? (inline_prefix ? 5 : 6) : 4);
     return CP_OK;
 }
 
@@ -885,18 +970,20 @@ int launch_bricks_k(const Prepared &P, const OffsetList &L, float *V, cudaStream
     const bool vec = V && (g.nx % 4 == 0) && aligned(V, 16);
     const bool rel = !grid_points_exact(g);
     const unsigned nb = (unsigned)nbricks;
+    bool launched = false;
     if (counts && rel)
-        cutoff_brick_kernel<K, false, true, true><<<nb, kBrickThreads, 0, stream>>>(p);
+        launched = launch_pdl(cutoff_brick_kernel<K, false, true, true>, (int)nb, kBrickThreads, stream, p);
     else if (counts)
-        cutoff_brick_kernel<K, false, true, false><<<nb, kBrickThreads, 0, stream>>>(p);
+        launched = launch_pdl(cutoff_brick_kernel<K, false, true, false>, (int)nb, kBrickThreads, stream, p);
     else if (vec && rel)
-        cutoff_brick_kernel<K, true, false, true><<<nb, kBrickThreads, 0, stream>>>(p);
+        launched = launch_pdl(cutoff_brick_kernel<K, true, false, true>, (int)nb, kBrickThreads, stream, p);
     else if (vec)
-        cutoff_brick_kernel<K, true, false, false><<<nb, kBrickThreads, 0, stream>>>(p);
+        launched = launch_pdl(cutoff_brick_kernel<K, true, false, false>, (int)nb, kBrickThreads, stream, p);
     else if (rel)
-        cutoff_brick_kernel<K, false, false, true><<<nb, kBrickThreads, 0, stream>>>(p);
+        launched = launch_pdl(cutoff_brick_kernel<K, false, false, true>, (int)nb, kBrickThreads, stream, p);
     else
-        cutoff_brick_kernel<K, false, false, false><<<nb, kBrickThreads, 0, stream>>>(p);
+        launched = launch_pdl(cutoff_brick_kernel<K, false, false, false>, (int)nb, kBrickThreads, stream, p);
+    if (!launched) return CP_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
     note_launches(1);
     return CP_OK;

@@ -132,6 +132,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     return mbar_wait_limit(bar, parity, status, kWaitLimitNs);
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialization attribute may be scheduled while the kernel before
+// it on the stream is still running; pdl_wait() blocks until that kernel
+// has completed and its memory operations are visible, so it comes before
+// any global memory access.  pdl_launch_dependents() lets the next such
+// kernel start being scheduled.  Both are no-ops without a programmatic
+// dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 1-D bulk copy global -> this CTA's shared memory, completion counted on
 // `bar` in bytes.  dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
