@@ -382,7 +382,7 @@ constexpr int kBrickStages = 8;
 struct BrickParams {
     int nx, ny, nz;
     float ox, oy, oz, h;
-    float c2, cull2, gc0, gc1, gc2;
+    float c2, cull2, full2, gc0, gc1, gc2;
     int nb[3];
     int m;
     double h64, b64;
@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
             // the sub-box's point farthest from the atom is one of its corners
             const float fx = fmaxf(a.x - lox, hix - a.x), fy = fmaxf(a.y - loy, hiy - a.y);
             const float fz = fmaxf(a.z - loz, hiz - a.z);
-            const bool whole = near && fmaf(fz, fz, fmaf(fy, fy, fx * fx)) < p.c2;
+            const bool whole = near && fmaf(fz, fz, fmaf(fy, fy, fx * fx)) < p.full2;
             const unsigned mf = __ballot_sync(0xffffffffu, whole);
             const unsigned mp = __ballot_sync(0xffffffffu, near && !whole);
             const float4 entry = REL ? make_float4(p.ox - a.x, p.oy - a.y, p.oz - a.z, a.w) : a;
@@ -939,6 +939,19 @@ int launch_bricks_k(const Prepared &P, const OffsetList &L, float *V, cudaStream
     const double c = P.bg.c;
     p.c2 = (float)(c * c);
     p.cull2 = (float)(c * c * (1.0 + 1.0e-5));
+    // An atom is "full" (its pairs taken without the r < c test) only when
+    // it is inside c of every point of a sub-box by more than the rounding
+    // of the test: 1e-5 of c plus 8 ulps of the largest coordinate near the
+    // grid (the sub-box corners and the atoms are fp32 numbers of that size).
+    {
+        double mag = 0.0;
+        const double o[3] = {g.ox, g.oy, g.oz};
+        const int n[3] = {g.nx, g.ny, g.nz};
+        for (int d = 0; d < 3; ++d)
+            mag = std::max(mag, std::max(std::fabs(o[d]), std::fabs(o[d] + (n[d] - 1) * (double)g.h)) + c);
+        const double margin = 1.0e-5 * c + 8.0 * mag * std::ldexp(1.0, -24);
+        p.full2 = margin < c ? (float)((c - margin) * (c - margin)) : 0.0f;
+    }
     p.gc0 = (float)(15.0 / (8.0 * c));
     p.gc1 = (float)(-5.0 / (4.0 * c * c * c));
     p.gc2 = (float)(3.0 / (8.0 * c * c * c * c * c));

@@ -197,3 +197,45 @@ def test_cutoff_useful_pairs_exact(K, seed, n, shape, h, origin, c, b):
     lo, hi = _pairs_within(w, c, -2e-6), _pairs_within(w, c, 2e-6)
     assert lo <= counts["useful"] <= hi, (counts, lo, hi)
     assert counts["useful"] <= counts["evaluated"] <= counts["examined"]
+
+
+def _boundary_atoms(origin, h, c, rng):
+    """Atoms at distance c(1 + eps) from a corner of consumer-warp sub-boxes
+    (8 x 4 x 4 points of an 8x8x8 brick): along the sub-box diagonal from its
+    low corner (that corner is then the sub-box point farthest from the atom,
+    so the atom is within c of the whole sub-box iff c(1 + eps) < c), and
+    beyond its high corner (the nearest point).  eps spans -1e-3 .. 1e-3,
+    down to a few fp32 ulps either side of c."""
+    o = np.asarray(origin, dtype=np.float64)
+    atoms = []
+    for brick in ((0, 0, 0), (1, 1, 1), (2, 1, 0)):
+        for w in range(4):
+            lo = o + h * np.array([8 * brick[0], 8 * brick[1] + 4 * (w & 1), 8 * brick[2] + 4 * (w >> 1)])
+            hi = lo + h * np.array([7.0, 3.0, 3.0])
+            diag = (hi - lo) / np.linalg.norm(hi - lo)
+            for eps in (-1e-3, -1e-5, -1e-6, -1e-7, 0.0, 1e-7, 1e-6, 1e-5, 1e-3):
+                R = c * (1.0 + eps)
+                atoms.append(list(lo + R * diag) + [rng.uniform(-1, 1)])
+                atoms.append(list(hi + R * np.ones(3) / np.sqrt(3.0)) + [rng.uniform(-1, 1)])
+    return np.asarray(atoms, dtype=np.float32)
+
+
+@pytest.mark.parametrize("K", [0, 16])
+@pytest.mark.parametrize("offset,h", [(0.0, 0.5), (5000.0, 0.37)])
+def test_cutoff_atoms_on_the_full_boundary(K, offset, h):
+    """An atom just inside c of a whole sub-box takes the moments path (q/r per
+    pair, -q g(r) from the sub-box's charge moments), one just outside it the
+    per-pair switched term.  At every point the map must match the brute-force
+    oracle within the bound -- exactly 0 where no atom is strictly inside c --
+    on a grid at the coordinate origin and on one 5000 A out (differences
+    relative to the grid origin)."""
+    rng = np.random.default_rng(777)
+    c, b = 3.0, 1.0
+    origin = (offset + 0.0, -offset, offset / 2) if offset else (0.0, 0.0, 0.0)
+    origin = tuple(float(np.float32(v)) for v in origin)
+    atoms = _boundary_atoms(origin, float(np.float32(h)), c, rng)
+    w = workloads.Workload("full_boundary", atoms, (24, 24, 24), origin, h)
+    V = _run(w, c, b, K)
+    ref, bound = oracle.cutoff_brute(w.atoms, w.shape, w.origin, w.h, c)
+    assert (np.asarray(bound) == 0).any()  # points no atom reaches: V must be exactly 0 there
+    assert_within_bound(V.cpu().numpy(), ref, bound, f"full boundary K={K} offset={offset}")
