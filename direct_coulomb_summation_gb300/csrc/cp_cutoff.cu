@@ -803,25 +803,6 @@ __global__ void __launch_bounds__(kBrickThreads, 6) cutoff_brick_kernel(const __
 
 namespace {
 
-// Launches kernel<<<grid, block, 0, stream>>>(args...) with programmatic
-// stream serialization: it may be scheduled while the previous kernel on
-// the stream drains, and it waits for that kernel (pdl_wait) before
-// touching memory.
-template <typename... KArgs, typename... Args>
-bool launch_pdl(void (*kernel)(KArgs...), int grid, int block, cudaStream_t stream, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3((unsigned)block);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess;
-}
-
 // Kernel arguments of the binning kernels for the sections of `L` at `ws`.
 BinParams bin_params(const float4 *atoms, int n_atoms, const BinGeom &bg, const cp_cutoff_layout &L, void *workspace) {
     char *ws = static_cast<char *>(workspace);

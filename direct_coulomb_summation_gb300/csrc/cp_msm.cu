@@ -154,6 +154,8 @@ __device__ __forceinline__ void msm_store_pair(const MsmLevelDev &L, int x, int 
 // W(d) = g_c(|d| h0) - g_2c(|d| h0) for |d|^2 < (2c/h0)^2, else 0; and the
 // top-level table 2^-L g_c(sqrt(s) h0) for s = 0 .. 3*11^2.
 __global__ void msm_stencil_kernel(const __grid_constant__ MsmParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int side = 2 * p.R + 1;
     const int n = side * side * side;
     const long long stride = (long long)gridDim.x * blockDim.x;
@@ -181,6 +183,8 @@ __global__ void msm_stencil_kernel(const __grid_constant__ MsmParams p) {
 // Lattice coordinates t = (r - o)/h0 of every cell-sorted atom, once per
 // atom (the same fp32 expression as the cell index), with its charge.
 __global__ void __launch_bounds__(kMsmThreads) msm_tcoord_kernel(const __grid_constant__ MsmParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= p.cell_start[p.ncells]) return;
     const float4 a = p.cell_atoms[t];
@@ -191,6 +195,8 @@ __global__ void __launch_bounds__(kMsmThreads) msm_tcoord_kernel(const __grid_co
 // the atoms of the cells i-2 .. i+1 (per axis) of q Phi(t - i), in cell
 // order.  One thread per node, nodes x fastest.
 __global__ void __launch_bounds__(kMsmThreads) msm_anterp_kernel(const __grid_constant__ MsmParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const MsmLevelDev &L0 = p.lv[0];
     const long long total = (long long)L0.n[0] * L0.n[1] * L0.n[2];
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -235,6 +241,8 @@ __device__ __forceinline__ float msm_rw(int k) {
 // q(l+1) at every padded entry: zero in the padding, else
 // sum_k w(kx) w(ky) w(kz) q(l)[2J + k] over the fine nodes that exist.
 __global__ void __launch_bounds__(kMsmThreads) msm_restrict_kernel(const __grid_constant__ MsmParams p, int l) {
+    pdl_launch_dependents();
+    pdl_wait();
     const MsmLevelDev &F = p.lv[l];
     const MsmLevelDev &C = p.lv[l + 1];
     const long long total = (long long)C.qd[0] * C.qd[1] * C.qd[2];
@@ -349,6 +357,8 @@ __device__ __forceinline__ void msm_conv_tile(const MsmParams &p, const MsmLevel
 }
 
 __global__ void __launch_bounds__(kMsmThreads) msm_conv_kernel(const __grid_constant__ MsmParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     int l = 0;
     while (l + 2 < p.levels && (long long)blockIdx.x >= p.lv[l + 1].cta_begin) ++l;
     const MsmLevelDev &Lv = p.lv[l];
@@ -372,6 +382,8 @@ __global__ void __launch_bounds__(kMsmThreads) msm_conv_kernel(const __grid_cons
 // Top level: e_i = sum_j gtop[|i - j|^2] q_j over all top nodes; one warp
 // per node, lanes take every 32nd node, fixed-order reduction.
 __global__ void __launch_bounds__(kMsmThreads) msm_top_kernel(const __grid_constant__ MsmParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const MsmLevelDev &T = p.lv[p.levels - 1];
     const int nodes = T.n[0] * T.n[1] * T.n[2];
     const int node = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
@@ -420,6 +432,8 @@ __device__ __forceinline__ int msm_prolong_taps(int i, int J0[4], float w[4]) {
 // e(l) = 2^-l * (sum of the S partial sums, in split order) + the level-l+1
 // potentials interpolated to the level-l nodes.
 __global__ void __launch_bounds__(kMsmThreads) msm_reduce_prolong_kernel(const __grid_constant__ MsmParams p, int l) {
+    pdl_launch_dependents();
+    pdl_wait();
     const MsmLevelDev &F = p.lv[l];
     const MsmLevelDev &C = p.lv[l + 1];
     const long long nodes = (long long)F.n[0] * F.n[1] * F.n[2];
@@ -480,6 +494,8 @@ struct InterpParams {
 template <bool VEC>
 __global__ void __launch_bounds__(kMsmThreads) msm_interp_kernel(const __grid_constant__ MsmParams p,
                                                                   const __grid_constant__ InterpParams g) {
+    pdl_launch_dependents();
+    pdl_wait();
     const long long quad = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (quad >= g.quads) return;
     const int qx = (int)(quad % g.qx);
@@ -579,6 +595,8 @@ __global__ void __launch_bounds__(kMsmThreads) msm_interp_kernel(const __grid_co
 template <int SPAN>
 __global__ void __launch_bounds__(kMsmThreads) msm_interp_brick_kernel(const __grid_constant__ MsmParams p,
                                                                         const __grid_constant__ InterpParams g) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ float E[SPAN][SPAN][SPAN];     // [z][y][x] nodes around the brick
     __shared__ float S1[kBrick][SPAN][SPAN];  // [point z][node y][node x]
     __shared__ float S2[kBrick][kBrick][SPAN];  // [point z][point y][node x]
@@ -948,35 +966,35 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     unsigned long long launches = 0;
     const int side = 2 * L.radius + 1;
     const long long nst = (long long)side * side * side + kMsmTopTable;
-    msm_stencil_kernel<<<(unsigned)std::min<long long>((nst + 255) / 256, 1024), 256, 0, st>>>(p);
+    bool ok = launch_pdl(msm_stencil_kernel, (int)std::min<long long>((nst + 255) / 256, 1024), 256, st, p);
     const MsmLevelDev &L0 = p.lv[0];
     const long long q0n = (long long)L0.n[0] * L0.n[1] * L0.n[2];
     // the charge lattice's padding must be zero: clear it all, nodes follow
     if (cudaMemsetAsync(L0.q, 0, (size_t)8 * L0.plane * L0.qd[2], st) != cudaSuccess) return CP_ERR_CUDA;
     if (n_atoms > 0) {
-        msm_tcoord_kernel<<<(unsigned)((n_atoms + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p);
+        ok = ok && launch_pdl(msm_tcoord_kernel, (int)((n_atoms + kMsmThreads - 1) / kMsmThreads), kMsmThreads, st, p);
         ++launches;
     }
-    msm_anterp_kernel<<<(unsigned)((q0n + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p);
+    ok = ok && launch_pdl(msm_anterp_kernel, (int)((q0n + kMsmThreads - 1) / kMsmThreads), kMsmThreads, st, p);
     launches += 2;
     for (int l = 0; l + 1 < L.levels; ++l) {
         const MsmLevelDev &C = p.lv[l + 1];
         const long long qn = (long long)C.qd[0] * C.qd[1] * C.qd[2];
-        msm_restrict_kernel<<<(unsigned)((qn + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p, l);
+        ok = ok && launch_pdl(msm_restrict_kernel, (int)((qn + kMsmThreads - 1) / kMsmThreads), kMsmThreads, st, p, l);
         ++launches;
     }
     if (cta > 0) {
-        msm_conv_kernel<<<(unsigned)cta, kMsmThreads, 0, st>>>(p);
+        ok = ok && launch_pdl(msm_conv_kernel, (int)cta, kMsmThreads, st, p);
         ++launches;
     }
     const MsmLevelDev &T = p.lv[L.levels - 1];
     const long long tn = (long long)T.n[0] * T.n[1] * T.n[2];
-    msm_top_kernel<<<(unsigned)((tn * 32 + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p);
+    ok = ok && launch_pdl(msm_top_kernel, (int)((tn * 32 + kMsmThreads - 1) / kMsmThreads), kMsmThreads, st, p);
     ++launches;
     for (int l = L.levels - 2; l >= 0; --l) {
         const MsmLevelDev &F = p.lv[l];
         const long long fn = (long long)F.n[0] * F.n[1] * F.n[2] * (F.split >= 16 ? kReduceGroup : 1);
-        msm_reduce_prolong_kernel<<<(unsigned)((fn + kMsmThreads - 1) / kMsmThreads), kMsmThreads, 0, st>>>(p, l);
+        ok = ok && launch_pdl(msm_reduce_prolong_kernel, (int)((fn + kMsmThreads - 1) / kMsmThreads), kMsmThreads, st, p, l);
         ++launches;
     }
     InterpParams ip;
@@ -997,17 +1015,17 @@ CP_API int cp_msm_longrange(const float *atoms, int n_atoms, int nx, int ny, int
     // nodes a brick's 8 points need per axis: at most ceil(7 h / h0) + 4
     const int span = (int)std::ceil(7.0 * (double)g.h / (double)lattice_h + 1e-4) + 4;
     if (g.h <= lattice_h && span <= 6 && nbricks <= 0x7fffffffLL)
-        msm_interp_brick_kernel<6><<<(unsigned)nbricks, kMsmThreads, 0, st>>>(p, ip);
+        ok = ok && launch_pdl(msm_interp_brick_kernel<6>, (int)nbricks, kMsmThreads, st, p, ip);
     else if (g.h <= lattice_h && span <= 8 && nbricks <= 0x7fffffffLL)
-        msm_interp_brick_kernel<8><<<(unsigned)nbricks, kMsmThreads, 0, st>>>(p, ip);
+        ok = ok && launch_pdl(msm_interp_brick_kernel<8>, (int)nbricks, kMsmThreads, st, p, ip);
     else if (g.h <= lattice_h && span <= 12 && nbricks <= 0x7fffffffLL)
-        msm_interp_brick_kernel<12><<<(unsigned)nbricks, kMsmThreads, 0, st>>>(p, ip);
+        ok = ok && launch_pdl(msm_interp_brick_kernel<12>, (int)nbricks, kMsmThreads, st, p, ip);
     else if ((g.nx % 4 == 0) && aligned(V, 16))
-        msm_interp_kernel<true><<<iblocks, kMsmThreads, 0, st>>>(p, ip);
+        ok = ok && launch_pdl(msm_interp_kernel<true>, (int)iblocks, kMsmThreads, st, p, ip);
     else
-        msm_interp_kernel<false><<<iblocks, kMsmThreads, 0, st>>>(p, ip);
+        ok = ok && launch_pdl(msm_interp_kernel<false>, (int)iblocks, kMsmThreads, st, p, ip);
     ++launches;
-    if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
+    if (!ok || cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
     note_launches(launches);
     return CP_OK;
 }
