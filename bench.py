@@ -565,7 +565,7 @@ def run_ours(args):
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     hbm_basis = "of measured" if "hbm_gbs" in peaks else "of fallback"
 
-    # the cutoff leg again as one captured CUDA graph (binning's six launches
+    # the cutoff leg again as one captured CUDA graph (binning's five launches
     # and the map replayed without per-launch host overhead)
     t_graph_cut = None
     if do_cutoff:
