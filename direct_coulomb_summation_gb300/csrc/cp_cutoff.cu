@@ -32,7 +32,8 @@
 //     consumer warp tests all the stage's atoms against its own sub-box,
 //     copies those that can reach it into its own list (stage order),
 //     releases the stage and runs the list through the pair loop.  An atom
-//     within c of every point of the sub-box ("full") adds q * rsqrt(r^2)
+//     inside c of every point of the sub-box by more than the rounding of
+//     the test ("full") adds q * rsqrt(r^2)
 //     per pair; its -q g(r) is a quartic polynomial in the point's position,
 //     added once per point at the end from 15 charge moments of the full
 //     atoms about the sub-box centre.  Any other listed atom adds the
